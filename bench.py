@@ -1,0 +1,422 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 block-scaled grouped GEMM on GB300.
+
+One step = one grouped call (prologue + persistent GEMM kernel) over the
+workload's seeded synthetic inputs, resident in HBM, L2 flushed between timed
+calls. Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+N > 1 runs N independent replicas (one process per GPU under torchrun; the
+path has no exchange step); value = all ranks' FLOPs / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "µs per grouped call and dense FP4 TFLOPS; % of roofline (1×GB300)"
+FP4_OVER_BF16 = 13.5 / 2.25     # nominal dense FP4 : BF16 tensor rate on GB300
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+WORKLOAD_TEXT = {
+    "tiny": "G=2: (128,128,256), (64,256,256)",
+    "decode": "G=8 decode MoE: m_g~U[40,192], n=4096, k=7168",
+    "prefill": "G=8 prefill: m_g=1024, n=4096, k=7168",
+    "ragged": "G=4 ragged: m_g=(1,17,333,1000), n=7168, k=2048, B~N(0,0.02)+1% x50",
+    "zipf64": "G=64 Zipf(1.2) routing of 16384 tokens (60 active, 4 idle), n=2048, k=7168",
+}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default="decode", choices=list(WORKLOAD_TEXT))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--tile-n", type=int, default=0, help="GEMM tile N (0 = library default)")
+    ap.add_argument("--flush-mb", type=int, default=512, help="L2 flush buffer written between timed calls")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target wall time of the oracle sample")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ helpers
+
+def measured_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK), "fallback"
+
+
+def roofline_terms(flops, nbytes, peaks):
+    """Roofline of one grouped call: time = max(FLOPs at the FP4 peak, bytes at HBM)."""
+    fp4_tflops = peaks["bf16_tflops"] * FP4_OVER_BF16
+    t_flop = flops / (fp4_tflops * 1e12)
+    t_mem = nbytes / (peaks["hbm_gbs"] * 1e9)
+    return ("tensor" if t_flop >= t_mem else "hbm"), t_flop, t_mem, fp4_tflops
+
+
+def stored_traffic(workload, tile_n):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel source as it is now (else None)."""
+    import hashlib
+    summ = ROOT / "profiles" / f"gemm_kernel_{workload}.txt"
+    if not summ.exists():
+        return None
+    src = ROOT / "nvfp4_block_scaled_grouped_gb300" / "csrc" / "gemm.cu"
+    digest = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    kv = {}
+    for line in summ.read_text().splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("gemm.cu sha256[:16]") != digest or kv.get("tile_n") != str(tile_n):
+        return None
+    try:
+        return float(kv["dram bytes per launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        for line in Path(self.path).read_text().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        smax = [num(r[1]) for r in rows if num(r[1]) is not None]
+        pw = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower().startswith("active")})
+        # samples under load: power above the run's midpoint between min and max
+        if pw:
+            mid = (min(pw) + max(pw)) / 2
+            loaded = [float(r[0]) for r in rows if num(r[2]) is not None and num(r[2]) >= mid and num(r[0])]
+        else:
+            loaded = sm
+        return {"sm_mhz": statistics.median(loaded or sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+def gpu_uuid(dev_index):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        return u if u.startswith("GPU-") else f"GPU-{u}"
+    except Exception:
+        return str(dev_index)
+
+
+# ------------------------------------------------------------------ the oracle legs (CPU)
+
+def oracle_sample(prob, seconds, seed=1234):
+    """Time the CPU oracle on a column slice of every non-empty group, sized to
+    take about `seconds` of wall time. Returns (flops, wall_s, cores, text)."""
+    import numpy as np
+    from oracle import oracle
+
+    groups = [(g, s) for g, s in enumerate(prob.problem_sizes) if s[0] > 0 and s[1] > 0 and s[2] > 0]
+
+    def run(cols_per_group):
+        flops = 0.0
+        t0 = time.perf_counter()
+        for g, (m, n, k, _) in groups:
+            c = min(cols_per_group, n)
+            rows = np.repeat(np.arange(m, dtype=np.int32), c)
+            cols = np.tile(np.arange(c, dtype=np.int32), m)
+            oracle.gemm_sampled(m, n, k, prob.A[g], prob.B[g], prob.SFA[g], prob.SFB[g], rows, cols)
+            flops += 2.0 * m * c * k
+        return flops, time.perf_counter() - t0
+
+    f0, t0 = run(2)
+    per_col = t0 / 2
+    cols = int(max(2, min(max(s[1] for _, s in groups), seconds / max(per_col, 1e-9))))
+    flops, wall = run(cols)
+    text = (f"all rows x the first {cols} columns of each of the {len(groups)} non-empty groups "
+            f"({flops / 2:.3g} multiply-adds, fp64, full k)")
+    return flops, wall, oracle.max_threads(), text
+
+
+def reference_arm(args, rank, world):
+    """--impl reference: the CPU oracle, as it stands, on bounded samples."""
+    if rank != 0:
+        return 0
+    from nvfp4_block_scaled_grouped_gb300 import workloads
+    prob = workloads.make_problem(args.workload, seed=args.seed)
+    per_step = max(0.5, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(prob, per_step)
+    flops_l, wall_l = [], []
+    text, cores = "", 0
+    for _ in range(args.steps):
+        f, w, cores, text = oracle_sample(prob, per_step)
+        flops_l.append(f)
+        wall_l.append(w)
+    value = sum(flops_l) / sum(wall_l) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(wall_l) / len(wall_l),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args, prob),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {text}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(args, prob):
+    return {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
+            "group_count": prob.group_count,
+            "problem_sizes": [list(s) for s in prob.problem_sizes],
+            "sum_m": int(sum(s[0] for s in prob.problem_sizes)),
+            "seed": args.seed,
+            "l2": f"flushed between timed calls ({args.flush_mb} MB write)"}
+
+
+# ------------------------------------------------------------------ the GPU arm
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import nvfp4_block_scaled_grouped_gb300 as nv
+    from nvfp4_block_scaled_grouped_gb300 import workloads
+    from nvfp4_block_scaled_grouped_gb300.device import DeviceProblem
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    nv.lib()
+    if args.tile_n:
+        nv.set_tile_n(args.tile_n)
+    prob = workloads.make_problem(args.workload, seed=args.seed)
+    flops = prob.flops()
+    nbytes = prob.algorithmic_bytes()
+
+    stream = torch.cuda.current_stream(dev)
+    t_pack0 = torch.cuda.Event(enable_timing=True)
+    t_pack1 = torch.cuda.Event(enable_timing=True)
+    t_pack0.record(stream)
+    dp = DeviceProblem.upload(prob, device=dev)   # uploads, then packs scales with the library kernel
+    t_pack1.record(stream)
+    torch.cuda.synchronize()
+
+    flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=dev)
+    for _ in range(max(3, args.warmup)):
+        dp.run(stream)
+    torch.cuda.synchronize()
+    assert nv.device_status(stream) == 0, "a bounded wait gave up during warm-up"
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(gpu_uuid(local_rank)) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()                    # evict A/B/scales from L2 (outside the timed events)
+            ev[i][0].record(stream)
+            dp.run(stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        wall = time.perf_counter() - wall0
+    times_ms = [a.elapsed_time(b) for a, b in ev]
+    assert nv.device_status(stream) == 0, "a bounded wait gave up during the timed run"
+    t_ms = statistics.fmean(times_ms)
+    t_max = t_ms
+    if world > 1:
+        t = torch.tensor([t_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    value = world * flops / (t_max * 1e-3) / 1e12
+
+    # ---- e2e: host buffers in pinned memory, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        host_in = []
+        dev_in = []
+        for lst in (dp.A, dp.B, dp.SFA, dp.SFB):
+            for t in lst:
+                if t.numel():
+                    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                    h.copy_(t)
+                    host_in.append(h)
+                    dev_in.append(t)
+        host_out = [torch.empty(c.shape, dtype=c.dtype, pin_memory=True) for c in dp.C]
+        h2d = sum(h.numel() * h.element_size() for h in host_in)
+        d2h = sum(h.numel() * h.element_size() for h in host_out)
+        e2e_steps = max(3, min(args.steps, 10))
+        for _ in range(2):
+            for h, d in zip(host_in, dev_in):
+                d.copy_(h, non_blocking=True)
+            dp.run(stream)
+            for h, c in zip(host_out, dp.C):
+                h.copy_(c, non_blocking=True)
+        torch.cuda.synchronize()
+        e_ms = []
+        for _ in range(e2e_steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for h, d in zip(host_in, dev_in):
+                d.copy_(h, non_blocking=True)
+            dp.run(stream)
+            for h, c in zip(host_out, dp.C):
+                h.copy_(c, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            e_ms.append(a.elapsed_time(b))
+        em = statistics.fmean(e_ms)
+        if world > 1:
+            t = torch.tensor([em], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            em = float(t.item())
+        e2e = {"value": world * flops / (em * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": em, "steps": e2e_steps}
+
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = measured_peaks()
+    bound, t_flop, t_mem, fp4_peak = roofline_terms(flops, nbytes, peaks)
+    t_s = t_ms * 1e-3
+    tile_n = args.tile_n or 128
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": nbytes / t_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / t_s / 1e12, "peak": fp4_peak, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = stored_traffic(args.workload, tile_n)
+    roof["peak_source"] = (f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback") + \
+        ("" if bound == "hbm" else " bf16 burst x 6 (nominal FP4:BF16)")
+    roof["kernel"] = "prologue_kernel + grouped_gemm_kernel (one grouped call, events around both)"
+    roof["roofline_us"] = max(t_flop, t_mem) * 1e6
+    roof["frac_of_roofline_time"] = max(t_flop, t_mem) / t_s
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        f, w, cores, text = oracle_sample(prob, args.cpu_seconds)
+        cpu = {"value": f / w / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": text, "wall_s": w}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max, "us_per_call": t_max * 1e3,
+        "us_per_call_p10_p50_p90": [float(v * 1e3) for v in _pcts(times_ms)],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4 (e2m1 x e2m1, e4m3 per-16 scales) -> f32 acc -> f16",
+        "data": "synthetic (seeded N(0,1) -> NVFP4 per-16 quantisation)",
+        "config": dict(workload_config(args, prob), tile_n=tile_n, parallelism=f"replicas x{world}"),
+        "flops_per_call": flops, "bytes_per_call": nbytes,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "scale_pack_us": 1e3 * t_pack0.elapsed_time(t_pack1),
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _pcts(v):
+    s = sorted(v)
+    pick = lambda q: s[min(len(s) - 1, int(q * (len(s) - 1) + 0.5))]
+    return pick(0.1), pick(0.5), pick(0.9)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        return gpu_arm(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

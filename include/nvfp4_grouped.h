@@ -1,0 +1,131 @@
+/*
+ * nvfp4_grouped.h -- C ABI of the GB300 (sm_103a) NVFP4 block-scaled grouped GEMM.
+ *
+ * For every group g with m, n > 0 the library computes
+ *
+ *     C_g[i][j] = fp16( sum_k e2m1(A_g[i][k]) * e4m3(SFA_g[i][k/16])
+ *                             * e2m1(B_g[j][k]) * e4m3(SFB_g[j][k/16]) )
+ *
+ * on the tensor cores (tcgen05 block-scaled MMA, fp32 accumulation, one
+ * round-to-nearest-even conversion to fp16). This is the problem of the
+ * kernelindex.com "nvfp4 group gemm" submissions 506336, 385043 and 499344:
+ * the entry point there takes per-group (a, b, c) tensors, per-group reordered
+ * (sfa, sfb) scale tensors and per-group (m, n, k, l) sizes, and writes each c
+ * in place (submission 499344, custom_kernel and its docstring; element types
+ * in submission 506336's module-level kernel configuration).
+ *
+ * Conventions shared by all entry points
+ * --------------------------------------
+ *  - Every device pointer is a CUDA device address on the current device.
+ *    Every call is asynchronous on `stream` (a cudaStream_t; 0 = legacy
+ *    default stream), never synchronises, and keeps no pointer after it
+ *    returns. The caller owns every buffer.
+ *  - Return value: NVFP4_OK (0) or a negative nvfp4_status. Argument errors
+ *    are detected on the host before anything is enqueued.
+ *  - Thread safety: calls may come from several host threads; calls on the
+ *    same stream are ordered by the stream.
+ */
+#ifndef NVFP4_GROUPED_H
+#define NVFP4_GROUPED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st *nvfp4_stream_t;
+
+/* Per-group problem size, as in the submissions' problem_sizes list: (m, n, k, l).
+ * l is the batch count of the group and must be 1 for non-empty groups
+ * (submission 499344 docstring: l is always 1). */
+typedef struct nvfp4_problem_size {
+    int32_t m, n, k, l;
+} nvfp4_problem_size;
+
+typedef enum nvfp4_status {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = -1, /* null array, negative size, null pointer in a non-empty group, too many groups */
+    NVFP4_ERR_UNSUPPORTED = -2, /* l != 1, k % 32 != 0 or n % 32 != 0 in a non-empty group, sizes too large */
+    NVFP4_ERR_MISALIGNED = -3,  /* a pointer of a non-empty group is not 16-byte aligned */
+    NVFP4_ERR_CUDA = -4,        /* a CUDA runtime/driver call or a launch failed */
+    NVFP4_ERR_TIMEOUT = -5      /* a kernel's bounded wait ran out (reported by nvfp4_device_status) */
+} nvfp4_status;
+
+/* Largest group_count accepted by nvfp4_grouped_gemm. */
+#define NVFP4_MAX_GROUPS 512
+
+/*
+ * nvfp4_grouped_gemm -- the grouped block-scaled GEMM.
+ *
+ * problem_sizes, A, B, SFA, SFB, C: HOST arrays of group_count entries. The
+ * pointer arrays hold DEVICE addresses:
+ *   A[g]   e2m1 codes, [m][k/2] bytes, K-major, two codes per byte (the even k
+ *          in the low nibble), row stride k/2 bytes.
+ *   B[g]   e2m1 codes, [n][k/2] bytes, same layout.
+ *   SFA[g] e4m3fn scales of A in the reordered atom layout, nvfp4_scale_bytes(m, k)
+ *          bytes: 512-byte atoms of 128 rows x 4 scale blocks, byte
+ *          16*(r%32) + 4*((r/32)%4) + (kb%4) inside atom (r/128)*ceil(k/64) + kb/4
+ *          (submission 385043, kernel body where the scale tensors are built);
+ *          padding rows/blocks must hold 0x00 (nvfp4_pack_scales writes them).
+ *          Scales must be non-negative and not NaN.
+ *   SFB[g] e4m3fn scales of B, nvfp4_scale_bytes(n, k) bytes, same layout.
+ *   C[g]   fp16, [m][n] row-major, written in full; nothing else is written.
+ * Group rules: a group with m == 0 or n == 0 is skipped and its pointers are
+ * not read (they may be null); a group with k == 0 and m, n > 0 gets C = +0.
+ * Non-empty groups need l == 1, k % 32 == 0, n % 32 == 0 and 16-byte aligned
+ * pointers (A, B, SFA, SFB may be null when k == 0).
+ * The library keeps a small device workspace per (device, stream), allocated
+ * on the first call for that pair and reused in stream order.
+ */
+int nvfp4_grouped_gemm(int group_count, const nvfp4_problem_size *problem_sizes,
+                       const void *const *A, const void *const *B,
+                       const void *const *SFA, const void *const *SFB,
+                       void *const *C, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_set_tile_n -- choose the BLOCK_N of the GEMM tile for later calls in
+ * this process: 128 or 256, or 0 to restore the automatic choice (128, or
+ * the NVFP4_TILE_N environment variable). Results do not depend on it.
+ * Returns NVFP4_OK or NVFP4_ERR_INVALID_ARG.
+ */
+int nvfp4_set_tile_n(int block_n);
+
+/*
+ * nvfp4_scale_bytes -- size of the reordered atom layout of a [rows][k/16]
+ * scale matrix: ceil(rows/128)*128 * ceil(k/64)*4 bytes. Returns 0 for
+ * rows <= 0 or k <= 0.
+ */
+size_t nvfp4_scale_bytes(int rows, int k);
+
+/*
+ * nvfp4_pack_scales -- reorder row-major scales into the atom layout.
+ *   sf_rowmajor  DEVICE, [rows][k/16] e4m3fn codes, row stride k/16 bytes.
+ *   sf_atoms     DEVICE, nvfp4_scale_bytes(rows, k) bytes; every byte is
+ *                written (padding = 0x00). Must not overlap sf_rowmajor.
+ * Requires rows >= 0, k >= 0, k % 16 == 0; rows == 0 or k == 0 is a no-op.
+ */
+int nvfp4_pack_scales(const void *sf_rowmajor, int rows, int k, void *sf_atoms,
+                      nvfp4_stream_t stream);
+
+/*
+ * nvfp4_device_status -- read and clear the device-side status word of the
+ * (current device, stream) workspace. Synchronises `stream`. *status receives
+ * NVFP4_OK, or NVFP4_ERR_TIMEOUT if a kernel of an earlier call gave up a
+ * bounded wait (its C is then incomplete). Returns NVFP4_OK or NVFP4_ERR_CUDA.
+ */
+int nvfp4_device_status(nvfp4_stream_t stream, int *status);
+
+/* Human-readable name of an nvfp4_status value (static string). */
+const char *nvfp4_status_string(int status);
+
+/* Detail of the last error returned on the calling host thread (static storage). */
+const char *nvfp4_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GROUPED_H */

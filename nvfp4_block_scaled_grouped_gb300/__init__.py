@@ -1,1 +1,155 @@
-"""NVFP4 block-scaled grouped GEMM for GB300 (sm_103a)."""
+"""NVFP4 block-scaled grouped GEMM for GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over the C ABI in ``include/nvfp4_grouped.h``
+(``_lib/libnvfp4_grouped.so``): argument marshalling only, every step of the
+computation runs in the library's CUDA kernels. There is no fallback: if the
+library is missing or fails to load, every call raises.
+
+The functions mirror the C entry points:
+
+* :func:`grouped_gemm` -- ``nvfp4_grouped_gemm`` (raw device pointers);
+* :func:`grouped_gemm_tensors` -- the same call taking torch CUDA tensors;
+* :func:`pack_scales` / :func:`scale_bytes` -- the scale-layout packer;
+* :func:`device_status`, :func:`set_tile_n`.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from pathlib import Path
+
+__all__ = [
+    "Nvfp4Error", "lib", "library_path", "grouped_gemm", "grouped_gemm_tensors", "pack_scales",
+    "pack_scales_tensor", "scale_bytes", "device_status", "set_tile_n", "MAX_GROUPS", "STATUS",
+]
+
+_PKG = Path(__file__).resolve().parent
+_LIB_PATH = _PKG / "_lib" / "libnvfp4_grouped.so"
+MAX_GROUPS = 512
+STATUS = {0: "NVFP4_OK", -1: "NVFP4_ERR_INVALID_ARG", -2: "NVFP4_ERR_UNSUPPORTED",
+          -3: "NVFP4_ERR_MISALIGNED", -4: "NVFP4_ERR_CUDA", -5: "NVFP4_ERR_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Nvfp4Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class ProblemSize(ctypes.Structure):
+    _fields_ = [("m", ctypes.c_int32), ("n", ctypes.c_int32), ("k", ctypes.c_int32), ("l", ctypes.c_int32)]
+
+
+def library_path() -> Path:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (once). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not _LIB_PATH.exists():
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(str(_LIB_PATH))
+        vp, vpp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)
+        L.nvfp4_grouped_gemm.restype = ctypes.c_int
+        L.nvfp4_grouped_gemm.argtypes = [ctypes.c_int, ctypes.POINTER(ProblemSize), vpp, vpp, vpp, vpp, vpp, vp]
+        L.nvfp4_scale_bytes.restype = ctypes.c_size_t
+        L.nvfp4_scale_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
+        L.nvfp4_pack_scales.restype = ctypes.c_int
+        L.nvfp4_pack_scales.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, vp]
+        L.nvfp4_device_status.restype = ctypes.c_int
+        L.nvfp4_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+        L.nvfp4_status_string.restype = ctypes.c_char_p
+        L.nvfp4_status_string.argtypes = [ctypes.c_int]
+        L.nvfp4_last_error_message.restype = ctypes.c_char_p
+        L.nvfp4_last_error_message.argtypes = []
+        L.nvfp4_set_tile_n.restype = ctypes.c_int
+        L.nvfp4_set_tile_n.argtypes = [ctypes.c_int]
+        _lib = L
+        return L
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise Nvfp4Error(status, lib().nvfp4_last_error_message().decode(errors="replace"))
+
+
+def _stream_handle(stream) -> int:
+    """A cudaStream_t value from None / int / torch.cuda.Stream."""
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _ptr_array(values):
+    arr = (ctypes.c_void_p * max(len(values), 1))()
+    for i, v in enumerate(values):
+        arr[i] = int(v) if v else None
+    return arr
+
+
+def grouped_gemm(problem_sizes, A, B, SFA, SFB, C, stream=None, *, check: bool = True) -> int:
+    """nvfp4_grouped_gemm with host lists of device addresses (ints)."""
+    G = len(problem_sizes)
+    sizes = (ProblemSize * max(G, 1))()
+    for g, (m, n, k, l) in enumerate(problem_sizes):
+        sizes[g] = ProblemSize(int(m), int(n), int(k), int(l))
+    status = lib().nvfp4_grouped_gemm(
+        G, sizes, _ptr_array(A), _ptr_array(B), _ptr_array(SFA), _ptr_array(SFB), _ptr_array(C),
+        ctypes.c_void_p(_stream_handle(stream) or None))
+    if check:
+        _check(status)
+    return status
+
+
+def _dptr(t):
+    return 0 if t is None or t.numel() == 0 else int(t.data_ptr())
+
+
+def grouped_gemm_tensors(problem_sizes, A, B, SFA, SFB, C, stream=None) -> None:
+    """Same call with torch CUDA tensors: A/B uint8 [rows, k/2], SFA/SFB uint8
+    atom-layout buffers, C float16 [m, n] (written in place)."""
+    grouped_gemm(problem_sizes, [_dptr(t) for t in A], [_dptr(t) for t in B], [_dptr(t) for t in SFA],
+                 [_dptr(t) for t in SFB], [_dptr(t) for t in C], stream)
+
+
+def scale_bytes(rows: int, k: int) -> int:
+    return int(lib().nvfp4_scale_bytes(int(rows), int(k)))
+
+
+def pack_scales(sf_rowmajor_ptr: int, rows: int, k: int, sf_atoms_ptr: int, stream=None) -> None:
+    _check(lib().nvfp4_pack_scales(ctypes.c_void_p(int(sf_rowmajor_ptr) or None), int(rows), int(k),
+                                   ctypes.c_void_p(int(sf_atoms_ptr) or None),
+                                   ctypes.c_void_p(_stream_handle(stream) or None)))
+
+
+def pack_scales_tensor(sf_rowmajor, k: int, stream=None):
+    """Device uint8 [rows, k/16] -> new device uint8 tensor in the atom layout."""
+    import torch
+    rows = sf_rowmajor.shape[0]
+    out = torch.empty(scale_bytes(rows, k), dtype=torch.uint8, device=sf_rowmajor.device)
+    if out.numel():
+        pack_scales(sf_rowmajor.data_ptr(), rows, k, out.data_ptr(), stream)
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Read and clear the device status word of this stream's workspace."""
+    st = ctypes.c_int(0)
+    _check(lib().nvfp4_device_status(ctypes.c_void_p(_stream_handle(stream) or None), ctypes.byref(st)))
+    return int(st.value)
+
+
+def set_tile_n(block_n: int) -> None:
+    _check(lib().nvfp4_set_tile_n(int(block_n)))

@@ -1,0 +1,307 @@
+// api.cu -- the C ABI: argument checks, per-device TMA descriptor templates,
+// per-(device, stream) workspaces, launch configuration.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "internal.h"
+
+namespace nvfp4 {
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int status, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(NVFP4_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    CUtensorMap tmpl_a;       // box 128 B x 128 rows
+    CUtensorMap tmpl_b128;    // box 128 B x 128 rows
+    CUtensorMap tmpl_b256;    // box 128 B x 256 rows
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+std::map<std::pair<int, cudaStream_t>, void *> g_workspaces;
+int g_tile_n_override = 0;
+
+// Encode a 2-D uint8 tensor map with 128-byte swizzle: dims {row_bytes, rows},
+// box {128 bytes, box_rows}. Out-of-bounds elements read as zero.
+int encode_template(EncodeTiledFn encode, CUtensorMap *out, void *addr, uint32_t box_rows) {
+    const cuuint64_t dims[2] = {128, 256};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t elem[2] = {1, 1};
+    CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, addr, dims, strides, box, elem,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return NVFP4_OK;
+}
+
+// Caller holds g_mutex.
+int device_state(int device, void *any_device_buffer, DeviceState **out) {
+    if (device < 0 || device >= kMaxDevices)
+        return fail(NVFP4_ERR_UNSUPPORTED, "device ordinal %d out of range", device);
+    DeviceState &st = g_devices[device];
+    if (!st.ready) {
+        cudaDeviceProp prop;
+        cudaError_t e = cudaGetDeviceProperties(&prop, device);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetDeviceProperties");
+        if (prop.major != 10 || prop.minor != 3)
+            return fail(NVFP4_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", device,
+                        prop.major, prop.minor);
+        st.sm_count = prop.multiProcessorCount;
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || fn == nullptr || q != cudaDriverEntryPointSuccess)
+            return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+        auto encode = reinterpret_cast<EncodeTiledFn>(fn);
+        int s = encode_template(encode, &st.tmpl_a, any_device_buffer, 128);
+        if (s == NVFP4_OK)
+            s = encode_template(encode, &st.tmpl_b128, any_device_buffer, 128);
+        if (s == NVFP4_OK)
+            s = encode_template(encode, &st.tmpl_b256, any_device_buffer, 256);
+        if (s != NVFP4_OK)
+            return s;
+        e = prepare_gemm_kernels(device);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaFuncSetAttribute");
+        st.ready = true;
+    }
+    *out = &st;
+    return NVFP4_OK;
+}
+
+// Caller holds g_mutex.
+int stream_workspace(int device, cudaStream_t stream, void **out) {
+    auto key = std::make_pair(device, stream);
+    auto it = g_workspaces.find(key);
+    if (it != g_workspaces.end()) {
+        *out = it->second;
+        return NVFP4_OK;
+    }
+    void *p = nullptr;
+    const size_t bytes = workspace_bytes(NVFP4_MAX_GROUPS);
+    cudaError_t e = cudaMalloc(&p, bytes);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMalloc(workspace)");
+    e = cudaMemset(p, 0, bytes);
+    if (e != cudaSuccess) {
+        cudaFree(p);
+        return cuda_fail(e, "cudaMemset(workspace)");
+    }
+    g_workspaces[key] = p;
+    *out = p;
+    return NVFP4_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+uint64_t watchdog_ns() {
+    const char *s = std::getenv("NVFP4_WATCHDOG_MS");
+    long long ms = s ? std::atoll(s) : 0;
+    if (ms <= 0)
+        ms = 4000;
+    return (uint64_t)ms * 1000000ull;
+}
+
+// BLOCK_N for a call: an explicit nvfp4_set_tile_n() value or NVFP4_TILE_N,
+// else 128.
+int choose_block_n() {
+    if (g_tile_n_override == 128 || g_tile_n_override == 256)
+        return g_tile_n_override;
+    const char *s = std::getenv("NVFP4_TILE_N");
+    if (s && std::atoi(s) == 256)
+        return 256;
+    return 128;
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+const char *nvfp4_status_string(int status) {
+    switch (status) {
+    case NVFP4_OK: return "NVFP4_OK";
+    case NVFP4_ERR_INVALID_ARG: return "NVFP4_ERR_INVALID_ARG";
+    case NVFP4_ERR_UNSUPPORTED: return "NVFP4_ERR_UNSUPPORTED";
+    case NVFP4_ERR_MISALIGNED: return "NVFP4_ERR_MISALIGNED";
+    case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA";
+    case NVFP4_ERR_TIMEOUT: return "NVFP4_ERR_TIMEOUT";
+    default: return "NVFP4_ERR_UNKNOWN";
+    }
+}
+
+const char *nvfp4_last_error_message(void) { return g_last_error; }
+
+size_t nvfp4_scale_bytes(int rows, int k) {
+    if (rows <= 0 || k <= 0)
+        return 0;
+    return (size_t)((rows + 127) / 128) * 128u * (size_t)((k + 63) / 64) * 4u;
+}
+
+int nvfp4_set_tile_n(int block_n) {
+    if (block_n != 0 && block_n != 128 && block_n != 256)
+        return fail(NVFP4_ERR_INVALID_ARG, "tile N must be 0 (automatic), 128 or 256, got %d", block_n);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_tile_n_override = block_n;
+    return NVFP4_OK;
+}
+
+int nvfp4_grouped_gemm(int group_count, const nvfp4_problem_size *problem_sizes, const void *const *A,
+                       const void *const *B, const void *const *SFA, const void *const *SFB, void *const *C,
+                       nvfp4_stream_t stream) {
+    if (group_count < 0)
+        return fail(NVFP4_ERR_INVALID_ARG, "group_count %d < 0", group_count);
+    if (group_count == 0)
+        return NVFP4_OK;
+    if (group_count > NVFP4_MAX_GROUPS)
+        return fail(NVFP4_ERR_INVALID_ARG, "group_count %d > %d", group_count, NVFP4_MAX_GROUPS);
+    if (!problem_sizes || !A || !B || !SFA || !SFB || !C)
+        return fail(NVFP4_ERR_INVALID_ARG, "null problem_sizes or pointer array");
+
+    const int block_n = choose_block_n();
+    GroupArgs args[NVFP4_MAX_GROUPS];
+    long long total = 0;
+    for (int g = 0; g < group_count; ++g) {
+        const nvfp4_problem_size &s = problem_sizes[g];
+        if (s.m < 0 || s.n < 0 || s.k < 0 || s.l < 0)
+            return fail(NVFP4_ERR_INVALID_ARG, "group %d: negative size (%d, %d, %d, %d)", g, s.m, s.n, s.k, s.l);
+        args[g] = GroupArgs{s.m, s.n, s.k, s.l, A[g], B[g], SFA[g], SFB[g], C[g]};
+        if (s.m == 0 || s.n == 0)
+            continue;
+        if (s.l != 1)
+            return fail(NVFP4_ERR_UNSUPPORTED, "group %d: l = %d (only l = 1 is supported)", g, s.l);
+        if (s.k % 32 != 0 || s.n % 32 != 0)
+            return fail(NVFP4_ERR_UNSUPPORTED, "group %d: k = %d and n = %d must be multiples of 32", g, s.k, s.n);
+        if (!C[g])
+            return fail(NVFP4_ERR_INVALID_ARG, "group %d: null C", g);
+        if (!aligned16(C[g]))
+            return fail(NVFP4_ERR_MISALIGNED, "group %d: C not 16-byte aligned", g);
+        if (s.k > 0) {
+            if (!A[g] || !B[g] || !SFA[g] || !SFB[g])
+                return fail(NVFP4_ERR_INVALID_ARG, "group %d: null A/B/SFA/SFB", g);
+            if (!aligned16(A[g]) || !aligned16(B[g]) || !aligned16(SFA[g]) || !aligned16(SFB[g]))
+                return fail(NVFP4_ERR_MISALIGNED, "group %d: A/B/SFA/SFB not 16-byte aligned", g);
+        }
+        total += (long long)((s.m + kBlockM - 1) / kBlockM) * (long long)((s.n + block_n - 1) / block_n);
+        if (total > 0x7fffffffLL)
+            return fail(NVFP4_ERR_UNSUPPORTED, "more than 2^31 - 1 tiles");
+    }
+    if (total == 0)
+        return NVFP4_OK;
+
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    DeviceState *st = nullptr;
+    void *ws_base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        int s = stream_workspace(device, reinterpret_cast<cudaStream_t>(stream), &ws_base);
+        if (s != NVFP4_OK)
+            return s;
+        s = device_state(device, ws_base, &st);
+        if (s != NVFP4_OK)
+            return s;
+    }
+    GemmLaunch cfg;
+    cfg.block_n = block_n;
+    cfg.group_count = group_count;
+    cfg.total_tiles = (int)total;
+    cfg.grid = (int)(total < st->sm_count ? total : st->sm_count);
+    cfg.timeout_ns = watchdog_ns();
+    const WorkspaceView ws = workspace_view(ws_base, NVFP4_MAX_GROUPS);
+    const void *tmpl_b = block_n == 256 ? (const void *)&st->tmpl_b256 : (const void *)&st->tmpl_b128;
+    e = launch_grouped(cfg, args, ws, &st->tmpl_a, tmpl_b, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "grouped GEMM launch");
+    return NVFP4_OK;
+}
+
+int nvfp4_pack_scales(const void *sf_rowmajor, int rows, int k, void *sf_atoms, nvfp4_stream_t stream) {
+    if (rows < 0 || k < 0)
+        return fail(NVFP4_ERR_INVALID_ARG, "negative rows (%d) or k (%d)", rows, k);
+    if (k % 16 != 0)
+        return fail(NVFP4_ERR_UNSUPPORTED, "k = %d is not a multiple of 16", k);
+    if (rows == 0 || k == 0)
+        return NVFP4_OK;
+    if (!sf_rowmajor || !sf_atoms)
+        return fail(NVFP4_ERR_INVALID_ARG, "null scale pointer");
+    if (!aligned16(sf_atoms))
+        return fail(NVFP4_ERR_MISALIGNED, "sf_atoms not 16-byte aligned");
+    cudaError_t e = launch_pack_scales(static_cast<const uint8_t *>(sf_rowmajor), rows, k,
+                                       static_cast<uint8_t *>(sf_atoms), reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "scale packer launch");
+    return NVFP4_OK;
+}
+
+int nvfp4_device_status(nvfp4_stream_t stream, int *status) {
+    if (!status)
+        return fail(NVFP4_ERR_INVALID_ARG, "null status");
+    *status = NVFP4_OK;
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    void *ws_base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        auto it = g_workspaces.find(std::make_pair(device, reinterpret_cast<cudaStream_t>(stream)));
+        if (it == g_workspaces.end())
+            return NVFP4_OK;
+        ws_base = it->second;
+    }
+    const WorkspaceView ws = workspace_view(ws_base, NVFP4_MAX_GROUPS);
+    uint32_t word = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    e = cudaMemcpyAsync(&word, ws.status, sizeof(word), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && word != 0) {
+        e = cudaMemsetAsync(ws.status, 0, sizeof(word), s);
+        if (e == cudaSuccess)
+            e = cudaStreamSynchronize(s);
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "reading the device status word");
+    if (word != 0) {
+        *status = NVFP4_ERR_TIMEOUT;
+        fail(NVFP4_ERR_TIMEOUT, "a bounded wait gave up (status bits 0x%x: 1 producer, 2 MMA, 4 epilogue)", word);
+    }
+    return NVFP4_OK;
+}
+
+}  // extern "C"

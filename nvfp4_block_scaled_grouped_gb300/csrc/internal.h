@@ -1,0 +1,101 @@
+// internal.h -- structures shared by the host layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "nvfp4_grouped.h"
+
+namespace nvfp4 {
+
+// Tile shape of one CTA: BLOCK_M rows of C (one 128-lane MMA), BLOCK_N columns
+// (a template parameter, 128 or 256), BLOCK_K = 256 fp4 elements = one
+// 128-byte swizzle row of packed codes = four MMAs of K = 64.
+constexpr int kBlockM = 128;
+constexpr int kBlockK = 256;
+constexpr int kMmaK = 64;
+constexpr int kSfAtomBytes = 512;  // 128 rows x 4 scale blocks
+
+// One group as the prologue writes it for the GEMM kernel (64 bytes).
+struct GroupInfo {
+    int32_t m, n, k;
+    int32_t tiles_m;        // ceil(m / BLOCK_M)
+    int32_t k_tiles;        // ceil(k / BLOCK_K)
+    int32_t k_blocks;       // ceil(k / 64): MMA k-blocks = scale atoms along K
+    int32_t sf_row_blocks_b;  // ceil(n / 128): 128-row scale blocks that exist for B
+    int32_t pad0;
+    const uint8_t *sfa;
+    const uint8_t *sfb;
+    void *c;
+    uint64_t pad1;
+};
+static_assert(sizeof(GroupInfo) == 64, "GroupInfo layout");
+
+// A group's raw arguments (host -> prologue, by kernel parameter).
+struct GroupArgs {
+    int32_t m, n, k, l;
+    const void *a, *b, *sfa, *sfb;
+    void *c;
+};
+
+// Device workspace, carved from one allocation at 128-byte aligned offsets.
+//   status   uint32 (bit flags of bounded waits that gave up)
+//   prefix   int32 [capacity + 1]  exclusive prefix sum of tiles per group
+//   groups   GroupInfo [capacity]
+//   tmaps    128-byte TMA descriptors [capacity][2] (A, B)
+struct WorkspaceView {
+    uint32_t *status;
+    int32_t *prefix;
+    GroupInfo *groups;
+    uint8_t *tmaps;
+    int32_t capacity;
+};
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline size_t workspace_bytes(int capacity) {
+    return 128 + round_up(sizeof(int32_t) * (size_t)(capacity + 1), 128) +
+           round_up(sizeof(GroupInfo) * (size_t)capacity, 128) + 256 * (size_t)capacity;
+}
+
+inline WorkspaceView workspace_view(void *base, int capacity) {
+    uint8_t *p = static_cast<uint8_t *>(base);
+    WorkspaceView v;
+    v.status = reinterpret_cast<uint32_t *>(p);
+    p += 128;
+    v.prefix = reinterpret_cast<int32_t *>(p);
+    p += round_up(sizeof(int32_t) * (size_t)(capacity + 1), 128);
+    v.groups = reinterpret_cast<GroupInfo *>(p);
+    p += round_up(sizeof(GroupInfo) * (size_t)capacity, 128);
+    v.tmaps = p;
+    v.capacity = capacity;
+    return v;
+}
+
+// Status bits written by the GEMM kernel when a bounded wait gives up.
+constexpr uint32_t kStatusProducerTimeout = 1u;
+constexpr uint32_t kStatusMmaTimeout = 2u;
+constexpr uint32_t kStatusEpilogueTimeout = 4u;
+
+// Launch configuration chosen by the host for one call.
+struct GemmLaunch {
+    int block_n;          // 128 or 256
+    int group_count;
+    int total_tiles;
+    int grid;             // persistent CTAs
+    uint64_t timeout_ns;  // bound of every mbarrier wait
+};
+
+// Host launchers (gemm.cu). `tmpl_a` / `tmpl_b` are 128-byte encoded TMA
+// descriptors used as templates by the prologue.
+cudaError_t launch_grouped(const GemmLaunch &cfg, const GroupArgs *groups, const WorkspaceView &ws,
+                           const void *tmpl_a, const void *tmpl_b, cudaStream_t stream);
+cudaError_t prepare_gemm_kernels(int device);
+size_t gemm_smem_bytes(int block_n);
+
+// Packer launcher (pack_scales.cu).
+cudaError_t launch_pack_scales(const uint8_t *src, int rows, int k, uint8_t *dst, cudaStream_t stream);
+
+}  // namespace nvfp4
