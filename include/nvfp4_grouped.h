@@ -85,6 +85,39 @@ int nvfp4_grouped_gemm(int group_count, const nvfp4_problem_size *problem_sizes,
                        const void *const *SFA, const void *const *SFB,
                        void *const *C, nvfp4_stream_t stream);
 
+/* Largest group_count accepted by nvfp4_grouped_gemm_noalloc. */
+#define NVFP4_NOALLOC_MAX_GROUPS 64
+
+/*
+ * nvfp4_grouped_gemm_noalloc -- nvfp4_grouped_gemm without any device
+ * allocation. The submissions have no counterpart: it exists for callers that
+ * must not have the library allocate device memory, such as frameworks that
+ * hand out every byte from their own pre-planned arena, and latency-critical
+ * callers that cannot afford a cudaMalloc (which may synchronise the whole
+ * device) in the middle of their work.
+ *
+ * Same arguments, layouts, results and error codes as nvfp4_grouped_gemm,
+ * except:
+ *  - at most NVFP4_NOALLOC_MAX_GROUPS (64) groups; more is rejected with
+ *    NVFP4_ERR_INVALID_ARG before anything is enqueued;
+ *  - the scratch (tile prefix sum, group table, TMA descriptors, status word;
+ *    about 21 KiB) is one fixed array in the library's device memory, which
+ *    every GPU that loads the library holds until the process exits. The call
+ *    never calls cudaMalloc, cudaFree or any other allocating routine;
+ *  - every call on a device shares that array and it keeps the previous
+ *    call's contents (each call rewrites what it reads and clears the status
+ *    word first). Calls whose work overlaps on the GPU -- on different
+ *    streams, or from different host threads without ordering -- race on it:
+ *    issue them in one stream or otherwise serialise them;
+ *  - the first call on a device sets that device up (looks up the array's
+ *    device address, encodes the TMA descriptor templates, sets kernel
+ *    attributes); make that first call before any stream capture begins.
+ */
+int nvfp4_grouped_gemm_noalloc(int group_count, const nvfp4_problem_size *problem_sizes,
+                               const void *const *A, const void *const *B,
+                               const void *const *SFA, const void *const *SFB,
+                               void *const *C, nvfp4_stream_t stream);
+
 /*
  * nvfp4_set_tile_n -- choose the BLOCK_N of the GEMM tile for later calls in
  * this process: 128 or 256, or 0 to restore the automatic choice (128, or

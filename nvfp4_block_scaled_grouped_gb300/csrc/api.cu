@@ -14,9 +14,10 @@
 #include "internal.h"
 
 namespace nvfp4 {
-namespace {
 
+namespace {
 thread_local char g_last_error[512] = "";
+}  // namespace
 
 int fail(int status, const char *fmt, ...) {
     va_list ap;
@@ -29,6 +30,8 @@ int fail(int status, const char *fmt, ...) {
 int cuda_fail(cudaError_t e, const char *what) {
     return fail(NVFP4_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
+
+namespace {
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -144,6 +147,78 @@ int choose_block_n() {
 }
 
 }  // namespace
+
+int check_groups(int group_count, int max_groups, const nvfp4_problem_size *problem_sizes, const void *const *A,
+                 const void *const *B, const void *const *SFA, const void *const *SFB, void *const *C, int block_n,
+                 GroupArgs *args, long long *total_tiles) {
+    *total_tiles = 0;
+    if (group_count < 0)
+        return fail(NVFP4_ERR_INVALID_ARG, "group_count %d < 0", group_count);
+    if (group_count == 0)
+        return NVFP4_OK;
+    if (group_count > max_groups)
+        return fail(NVFP4_ERR_INVALID_ARG, "group_count %d > %d", group_count, max_groups);
+    if (!problem_sizes || !A || !B || !SFA || !SFB || !C)
+        return fail(NVFP4_ERR_INVALID_ARG, "null problem_sizes or pointer array");
+    long long total = 0;
+    for (int g = 0; g < group_count; ++g) {
+        const nvfp4_problem_size &s = problem_sizes[g];
+        if (s.m < 0 || s.n < 0 || s.k < 0 || s.l < 0)
+            return fail(NVFP4_ERR_INVALID_ARG, "group %d: negative size (%d, %d, %d, %d)", g, s.m, s.n, s.k, s.l);
+        args[g] = GroupArgs{s.m, s.n, s.k, s.l, A[g], B[g], SFA[g], SFB[g], C[g]};
+        if (s.m == 0 || s.n == 0)
+            continue;
+        if (s.l != 1)
+            return fail(NVFP4_ERR_UNSUPPORTED, "group %d: l = %d (only l = 1 is supported)", g, s.l);
+        if (s.k % 32 != 0 || s.n % 32 != 0)
+            return fail(NVFP4_ERR_UNSUPPORTED, "group %d: k = %d and n = %d must be multiples of 32", g, s.k, s.n);
+        if (!C[g])
+            return fail(NVFP4_ERR_INVALID_ARG, "group %d: null C", g);
+        if (!aligned16(C[g]))
+            return fail(NVFP4_ERR_MISALIGNED, "group %d: C not 16-byte aligned", g);
+        if (s.k > 0) {
+            if (!A[g] || !B[g] || !SFA[g] || !SFB[g])
+                return fail(NVFP4_ERR_INVALID_ARG, "group %d: null A/B/SFA/SFB", g);
+            if (!aligned16(A[g]) || !aligned16(B[g]) || !aligned16(SFA[g]) || !aligned16(SFB[g]))
+                return fail(NVFP4_ERR_MISALIGNED, "group %d: A/B/SFA/SFB not 16-byte aligned", g);
+        }
+        total += (long long)((s.m + kBlockM - 1) / kBlockM) * (long long)((s.n + block_n - 1) / block_n);
+        if (total > 0x7fffffffLL)
+            return fail(NVFP4_ERR_UNSUPPORTED, "more than 2^31 - 1 tiles");
+    }
+    *total_tiles = total;
+    return NVFP4_OK;
+}
+
+int current_block_n() { return choose_block_n(); }
+
+int launch_on_workspace(int group_count, const GroupArgs *args, long long total_tiles, int block_n, void *ws_base,
+                        int capacity, cudaStream_t stream) {
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    DeviceState *st = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        int s = device_state(device, ws_base, &st);
+        if (s != NVFP4_OK)
+            return s;
+    }
+    GemmLaunch cfg;
+    cfg.block_n = block_n;
+    cfg.group_count = group_count;
+    cfg.total_tiles = (int)total_tiles;
+    cfg.grid = (int)(total_tiles < st->sm_count ? total_tiles : st->sm_count);
+    cfg.timeout_ns = watchdog_ns();
+    const WorkspaceView ws = workspace_view(ws_base, capacity);
+    const void *tmpl_b = block_n == 256 ? (const void *)&st->tmpl_b256 : (const void *)&st->tmpl_b128;
+    e = launch_grouped(cfg, args, ws, &st->tmpl_a, tmpl_b, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "grouped GEMM launch");
+    return NVFP4_OK;
+}
+
 }  // namespace nvfp4
 
 using namespace nvfp4;
@@ -181,73 +256,25 @@ int nvfp4_set_tile_n(int block_n) {
 int nvfp4_grouped_gemm(int group_count, const nvfp4_problem_size *problem_sizes, const void *const *A,
                        const void *const *B, const void *const *SFA, const void *const *SFB, void *const *C,
                        nvfp4_stream_t stream) {
-    if (group_count < 0)
-        return fail(NVFP4_ERR_INVALID_ARG, "group_count %d < 0", group_count);
-    if (group_count == 0)
-        return NVFP4_OK;
-    if (group_count > NVFP4_MAX_GROUPS)
-        return fail(NVFP4_ERR_INVALID_ARG, "group_count %d > %d", group_count, NVFP4_MAX_GROUPS);
-    if (!problem_sizes || !A || !B || !SFA || !SFB || !C)
-        return fail(NVFP4_ERR_INVALID_ARG, "null problem_sizes or pointer array");
-
     const int block_n = choose_block_n();
     GroupArgs args[NVFP4_MAX_GROUPS];
     long long total = 0;
-    for (int g = 0; g < group_count; ++g) {
-        const nvfp4_problem_size &s = problem_sizes[g];
-        if (s.m < 0 || s.n < 0 || s.k < 0 || s.l < 0)
-            return fail(NVFP4_ERR_INVALID_ARG, "group %d: negative size (%d, %d, %d, %d)", g, s.m, s.n, s.k, s.l);
-        args[g] = GroupArgs{s.m, s.n, s.k, s.l, A[g], B[g], SFA[g], SFB[g], C[g]};
-        if (s.m == 0 || s.n == 0)
-            continue;
-        if (s.l != 1)
-            return fail(NVFP4_ERR_UNSUPPORTED, "group %d: l = %d (only l = 1 is supported)", g, s.l);
-        if (s.k % 32 != 0 || s.n % 32 != 0)
-            return fail(NVFP4_ERR_UNSUPPORTED, "group %d: k = %d and n = %d must be multiples of 32", g, s.k, s.n);
-        if (!C[g])
-            return fail(NVFP4_ERR_INVALID_ARG, "group %d: null C", g);
-        if (!aligned16(C[g]))
-            return fail(NVFP4_ERR_MISALIGNED, "group %d: C not 16-byte aligned", g);
-        if (s.k > 0) {
-            if (!A[g] || !B[g] || !SFA[g] || !SFB[g])
-                return fail(NVFP4_ERR_INVALID_ARG, "group %d: null A/B/SFA/SFB", g);
-            if (!aligned16(A[g]) || !aligned16(B[g]) || !aligned16(SFA[g]) || !aligned16(SFB[g]))
-                return fail(NVFP4_ERR_MISALIGNED, "group %d: A/B/SFA/SFB not 16-byte aligned", g);
-        }
-        total += (long long)((s.m + kBlockM - 1) / kBlockM) * (long long)((s.n + block_n - 1) / block_n);
-        if (total > 0x7fffffffLL)
-            return fail(NVFP4_ERR_UNSUPPORTED, "more than 2^31 - 1 tiles");
-    }
-    if (total == 0)
-        return NVFP4_OK;
-
+    int s = check_groups(group_count, NVFP4_MAX_GROUPS, problem_sizes, A, B, SFA, SFB, C, block_n, args, &total);
+    if (s != NVFP4_OK || total == 0)
+        return s;
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaGetDevice");
-    DeviceState *st = nullptr;
     void *ws_base = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
-        int s = stream_workspace(device, reinterpret_cast<cudaStream_t>(stream), &ws_base);
-        if (s != NVFP4_OK)
-            return s;
-        s = device_state(device, ws_base, &st);
+        s = stream_workspace(device, reinterpret_cast<cudaStream_t>(stream), &ws_base);
         if (s != NVFP4_OK)
             return s;
     }
-    GemmLaunch cfg;
-    cfg.block_n = block_n;
-    cfg.group_count = group_count;
-    cfg.total_tiles = (int)total;
-    cfg.grid = (int)(total < st->sm_count ? total : st->sm_count);
-    cfg.timeout_ns = watchdog_ns();
-    const WorkspaceView ws = workspace_view(ws_base, NVFP4_MAX_GROUPS);
-    const void *tmpl_b = block_n == 256 ? (const void *)&st->tmpl_b256 : (const void *)&st->tmpl_b128;
-    e = launch_grouped(cfg, args, ws, &st->tmpl_a, tmpl_b, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess)
-        return cuda_fail(e, "grouped GEMM launch");
-    return NVFP4_OK;
+    return launch_on_workspace(group_count, args, total, block_n, ws_base, NVFP4_MAX_GROUPS,
+                               reinterpret_cast<cudaStream_t>(stream));
 }
 
 int nvfp4_pack_scales(const void *sf_rowmajor, int rows, int k, void *sf_atoms, nvfp4_stream_t stream) {

@@ -53,9 +53,9 @@ struct WorkspaceView {
     int32_t capacity;
 };
 
-inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+constexpr size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline size_t workspace_bytes(int capacity) {
+constexpr size_t workspace_bytes(int capacity) {
     return 128 + round_up(sizeof(int32_t) * (size_t)(capacity + 1), 128) +
            round_up(sizeof(GroupInfo) * (size_t)capacity, 128) + 256 * (size_t)capacity;
 }
@@ -94,6 +94,20 @@ cudaError_t launch_grouped(const GemmLaunch &cfg, const GroupArgs *groups, const
                            const void *tmpl_a, const void *tmpl_b, cudaStream_t stream);
 cudaError_t prepare_gemm_kernels(int device);
 size_t gemm_smem_bytes(int block_n);
+
+// Host layer (api.cu), shared by the entry points.
+int fail(int status, const char *fmt, ...);
+int cuda_fail(cudaError_t e, const char *what);
+// Check one call's arguments (at most max_groups groups); fills args[0..G)
+// and the tile count for a BLOCK_N of block_n.
+int check_groups(int group_count, int max_groups, const nvfp4_problem_size *problem_sizes, const void *const *A,
+                 const void *const *B, const void *const *SFA, const void *const *SFB, void *const *C, int block_n,
+                 GroupArgs *args, long long *total_tiles);
+int current_block_n();
+// Set up the current device on first use and launch a checked call whose
+// scratch is the workspace at ws_base (capacity groups).
+int launch_on_workspace(int group_count, const GroupArgs *args, long long total_tiles, int block_n, void *ws_base,
+                        int capacity, cudaStream_t stream);
 
 // Packer launcher (pack_scales.cu).
 cudaError_t launch_pack_scales(const uint8_t *src, int rows, int k, uint8_t *dst, cudaStream_t stream);
