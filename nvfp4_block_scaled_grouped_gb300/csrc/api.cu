@@ -48,7 +48,14 @@ struct DeviceState {
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
-std::map<std::pair<int, cudaStream_t>, void *> g_workspaces;
+// One workspace per (device, stream): base pointer, partial-tile slots and
+// the epoch of the last split call that used it.
+struct StreamWorkspace {
+    void *base = nullptr;
+    int partial_slots = 0;
+    uint32_t epoch = 0;
+};
+std::map<std::pair<int, cudaStream_t>, StreamWorkspace> g_workspaces;
 int g_tile_n_override = 0;
 
 // Encode a 2-D uint8 tensor map with 128-byte swizzle: dims {row_bytes, rows},
@@ -102,26 +109,34 @@ int device_state(int device, void *any_device_buffer, DeviceState **out) {
     return NVFP4_OK;
 }
 
-// Caller holds g_mutex.
-int stream_workspace(int device, cudaStream_t stream, void **out) {
+// Caller holds g_mutex. Allocates the workspace with `partial_slots`
+// partial-tile slots on first use for (device, stream).
+int stream_workspace(int device, cudaStream_t stream, int partial_slots, StreamWorkspace **out) {
     auto key = std::make_pair(device, stream);
     auto it = g_workspaces.find(key);
     if (it != g_workspaces.end()) {
-        *out = it->second;
+        *out = &it->second;
         return NVFP4_OK;
     }
     void *p = nullptr;
-    const size_t bytes = workspace_bytes(NVFP4_MAX_GROUPS);
+    const size_t bytes = workspace_bytes(NVFP4_MAX_GROUPS, partial_slots);
     cudaError_t e = cudaMalloc(&p, bytes);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMalloc(workspace)");
-    e = cudaMemset(p, 0, bytes);
+    // status word, prefix sums, group table, descriptors and flags start at
+    // zero; the partial tiles are always written before they are read
+    const size_t head = workspace_bytes(NVFP4_MAX_GROUPS, partial_slots) -
+                        kPartialSlotBytes * (size_t)partial_slots;
+    e = cudaMemset(p, 0, head);
     if (e != cudaSuccess) {
         cudaFree(p);
         return cuda_fail(e, "cudaMemset(workspace)");
     }
-    g_workspaces[key] = p;
-    *out = p;
+    StreamWorkspace &w = g_workspaces[key];
+    w.base = p;
+    w.partial_slots = partial_slots;
+    w.epoch = 0;
+    *out = &w;
     return NVFP4_OK;
 }
 
@@ -136,14 +151,15 @@ uint64_t watchdog_ns() {
 }
 
 // BLOCK_N for a call: an explicit nvfp4_set_tile_n() value or NVFP4_TILE_N,
-// else 128.
+// else 256 (a 128 x 256 x 64 MMA does twice the work of a 128 x 128 x 64 one
+// for about the same issue cost).
 int choose_block_n() {
     if (g_tile_n_override == 128 || g_tile_n_override == 256)
         return g_tile_n_override;
     const char *s = std::getenv("NVFP4_TILE_N");
-    if (s && std::atoi(s) == 256)
-        return 256;
-    return 128;
+    if (s && std::atoi(s) == 128)
+        return 128;
+    return 256;
 }
 
 }  // namespace
@@ -192,26 +208,55 @@ int check_groups(int group_count, int max_groups, const nvfp4_problem_size *prob
 
 int current_block_n() { return choose_block_n(); }
 
+// Split (stream-K) schedules pay off when there are few tiles per SM: with
+// whole tiles the last wave leaves SMs idle.
+bool want_split(long long total_tiles, int sm_count) {
+    const char *s = std::getenv("NVFP4_SPLIT");
+    if (s && *s)
+        return std::atoi(s) != 0;
+    return total_tiles < 4LL * sm_count;
+}
+
 int launch_on_workspace(int group_count, const GroupArgs *args, long long total_tiles, int block_n, void *ws_base,
-                        int capacity, cudaStream_t stream) {
+                        int capacity, int partial_slots, uint32_t *epoch, cudaStream_t stream) {
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaGetDevice");
     DeviceState *st = nullptr;
+    long long total_work = 0;
+    for (int g = 0; g < group_count; ++g) {
+        const GroupArgs &a = args[g];
+        if (a.m <= 0 || a.n <= 0)
+            continue;
+        const long long tiles = (long long)((a.m + kBlockM - 1) / kBlockM) * ((a.n + block_n - 1) / block_n);
+        const long long kt = (a.k + kBlockK - 1) / kBlockK;
+        total_work += tiles * (kt > 1 ? kt : 1);
+    }
+    if (total_work > 0x7fffffffLL)
+        return fail(NVFP4_ERR_UNSUPPORTED, "more than 2^31 - 1 k-tiles in one call");
+    GemmLaunch cfg;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         int s = device_state(device, ws_base, &st);
         if (s != NVFP4_OK)
             return s;
+        const int sms = st->sm_count;
+        cfg.split = (epoch != nullptr && partial_slots >= sms && want_split(total_tiles, sms)) ? 1 : 0;
+        if (cfg.split) {
+            cfg.grid = (int)(total_work < sms ? total_work : sms);
+            cfg.epoch = ++*epoch;
+        } else {
+            cfg.grid = (int)(total_tiles < sms ? total_tiles : sms);
+            cfg.epoch = 0;
+        }
     }
-    GemmLaunch cfg;
     cfg.block_n = block_n;
     cfg.group_count = group_count;
     cfg.total_tiles = (int)total_tiles;
-    cfg.grid = (int)(total_tiles < st->sm_count ? total_tiles : st->sm_count);
+    cfg.total_work = (int)total_work;
     cfg.timeout_ns = watchdog_ns();
-    const WorkspaceView ws = workspace_view(ws_base, capacity);
+    const WorkspaceView ws = workspace_view(ws_base, capacity, partial_slots);
     const void *tmpl_b = block_n == 256 ? (const void *)&st->tmpl_b256 : (const void *)&st->tmpl_b128;
     e = launch_grouped(cfg, args, ws, &st->tmpl_a, tmpl_b, stream);
     if (e != cudaSuccess)
@@ -266,15 +311,19 @@ int nvfp4_grouped_gemm(int group_count, const nvfp4_problem_size *problem_sizes,
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaGetDevice");
-    void *ws_base = nullptr;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    StreamWorkspace *w = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
-        s = stream_workspace(device, reinterpret_cast<cudaStream_t>(stream), &ws_base);
+        s = stream_workspace(device, reinterpret_cast<cudaStream_t>(stream), sms, &w);
         if (s != NVFP4_OK)
             return s;
     }
-    return launch_on_workspace(group_count, args, total, block_n, ws_base, NVFP4_MAX_GROUPS,
-                               reinterpret_cast<cudaStream_t>(stream));
+    return launch_on_workspace(group_count, args, total, block_n, w->base, NVFP4_MAX_GROUPS, w->partial_slots,
+                               &w->epoch, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int nvfp4_pack_scales(const void *sf_rowmajor, int rows, int k, void *sf_atoms, nvfp4_stream_t stream) {
@@ -309,7 +358,7 @@ int nvfp4_device_status(nvfp4_stream_t stream, int *status) {
         auto it = g_workspaces.find(std::make_pair(device, reinterpret_cast<cudaStream_t>(stream)));
         if (it == g_workspaces.end())
             return NVFP4_OK;
-        ws_base = it->second;
+        ws_base = it->second.base;
     }
     const WorkspaceView ws = workspace_view(ws_base, NVFP4_MAX_GROUPS);
     uint32_t word = 0;

@@ -25,9 +25,19 @@ def nv():
 
 
 @pytest.fixture(autouse=True)
-def _reset_tile(nv):
+def _reset_tile(nv, monkeypatch):
+    monkeypatch.delenv("NVFP4_SPLIT", raising=False)
     yield
     nv.set_tile_n(0)
+
+
+def _schedule(monkeypatch, split):
+    """split: None = library choice, True/False = force the split (stream-K)
+    or whole-tile schedule."""
+    if split is None:
+        monkeypatch.delenv("NVFP4_SPLIT", raising=False)
+    else:
+        monkeypatch.setenv("NVFP4_SPLIT", "1" if split else "0")
 
 
 def _run(nv, prob, block_n=128):
@@ -84,8 +94,12 @@ EDGE_SIZES = [
 ]
 
 
-@pytest.mark.parametrize("block_n", [128, 256])
-def test_edge_shapes_full(nv, oracle_mod, block_n):
+@pytest.mark.parametrize("block_n,split", [(128, False), (256, False), (128, True), (256, True)])
+def test_edge_shapes_full(nv, oracle_mod, monkeypatch, block_n, split):
+    """All edge shapes in one call; with the split schedule forced, the tiles
+    are cut along K over many CTAs (most pieces one k-tile long), so the
+    partial-tile hand-off between CTAs is exercised on every group."""
+    _schedule(monkeypatch, split)
     prob = _make(EDGE_SIZES, seed=3)
     dp, got = _run(nv, prob, block_n)
     ref = _oracle_full(oracle_mod, prob)
@@ -185,9 +199,11 @@ def _workload(name):
     return _PROBLEMS[name]
 
 
-@pytest.mark.parametrize("name,block_n", [("decode", 128), ("prefill", 128), ("prefill", 256),
-                                          ("ragged", 128), ("zipf64", 128)])
-def test_full_size_sampled(nv, oracle_mod, name, block_n):
+@pytest.mark.parametrize("name,block_n,split", [("decode", 256, None), ("decode", 128, False),
+                                                ("prefill", 256, None), ("prefill", 128, True),
+                                                ("ragged", 256, None), ("zipf64", 256, None)])
+def test_full_size_sampled(nv, oracle_mod, monkeypatch, name, block_n, split):
+    _schedule(monkeypatch, split)
     prob = _workload(name)
     dp, got = _run(nv, prob, block_n)
     rng = np.random.default_rng(17)
