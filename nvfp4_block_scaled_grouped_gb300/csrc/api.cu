@@ -52,8 +52,8 @@ DeviceState g_devices[kMaxDevices];
 // the epoch of the last split call that used it.
 struct StreamWorkspace {
     void *base = nullptr;
-    int partial_slots = 0;
-    uint32_t epoch = 0;
+    int slots = 0;  // CTA slots for prefix scratch and partial tiles
+    WorkspaceState state;
 };
 std::map<std::pair<int, cudaStream_t>, StreamWorkspace> g_workspaces;
 int g_tile_n_override = 0;
@@ -109,9 +109,9 @@ int device_state(int device, void *any_device_buffer, DeviceState **out) {
     return NVFP4_OK;
 }
 
-// Caller holds g_mutex. Allocates the workspace with `partial_slots`
-// partial-tile slots on first use for (device, stream).
-int stream_workspace(int device, cudaStream_t stream, int partial_slots, StreamWorkspace **out) {
+// Caller holds g_mutex. Allocates the workspace with `slots` per-CTA slots
+// (prefix scratch, partial tiles) on first use for (device, stream).
+int stream_workspace(int device, cudaStream_t stream, int slots, StreamWorkspace **out) {
     auto key = std::make_pair(device, stream);
     auto it = g_workspaces.find(key);
     if (it != g_workspaces.end()) {
@@ -119,14 +119,13 @@ int stream_workspace(int device, cudaStream_t stream, int partial_slots, StreamW
         return NVFP4_OK;
     }
     void *p = nullptr;
-    const size_t bytes = workspace_bytes(NVFP4_MAX_GROUPS, partial_slots);
+    const size_t bytes = workspace_bytes(NVFP4_MAX_GROUPS, slots, slots);
     cudaError_t e = cudaMalloc(&p, bytes);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMalloc(workspace)");
-    // status word, prefix sums, group table, descriptors and flags start at
-    // zero; the partial tiles are always written before they are read
-    const size_t head = workspace_bytes(NVFP4_MAX_GROUPS, partial_slots) -
-                        kPartialSlotBytes * (size_t)partial_slots;
+    // header (status word, descriptor counter), descriptors, prefix scratch
+    // and flags start at zero; partial tiles are written before they are read
+    const size_t head = bytes - kPartialSlotBytes * (size_t)slots;
     e = cudaMemset(p, 0, head);
     if (e != cudaSuccess) {
         cudaFree(p);
@@ -134,8 +133,8 @@ int stream_workspace(int device, cudaStream_t stream, int partial_slots, StreamW
     }
     StreamWorkspace &w = g_workspaces[key];
     w.base = p;
-    w.partial_slots = partial_slots;
-    w.epoch = 0;
+    w.slots = slots;
+    w.state = WorkspaceState();
     *out = &w;
     return NVFP4_OK;
 }
@@ -208,23 +207,27 @@ int check_groups(int group_count, int max_groups, const nvfp4_problem_size *prob
 
 int current_block_n() { return choose_block_n(); }
 
-// Split (stream-K) schedules pay off when there are few tiles per SM: with
-// whole tiles the last wave leaves SMs idle.
+// Split (stream-K) schedules pay off when whole tiles leave the last wave
+// mostly idle: ceil(T / P) waves against T / P waves of work. They cost
+// partial-tile traffic and an extra epilogue per split tile, so they are used
+// only when whole tiles would waste at least ~30% of the time.
 bool want_split(long long total_tiles, int sm_count) {
     const char *s = std::getenv("NVFP4_SPLIT");
     if (s && *s)
         return std::atoi(s) != 0;
-    return total_tiles < 4LL * sm_count;
+    const long long waves = (total_tiles + sm_count - 1) / sm_count;
+    return (double)waves >= 1.4 * (double)total_tiles / (double)sm_count;
 }
 
 int launch_on_workspace(int group_count, const GroupArgs *args, long long total_tiles, int block_n, void *ws_base,
-                        int capacity, int partial_slots, uint32_t *epoch, cudaStream_t stream) {
+                        int capacity, int prefix_slots, int partial_slots, WorkspaceState *state,
+                        cudaStream_t stream) {
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaGetDevice");
-    DeviceState *st = nullptr;
     long long total_work = 0;
+    int desc_groups = 0;
     for (int g = 0; g < group_count; ++g) {
         const GroupArgs &a = args[g];
         if (a.m <= 0 || a.n <= 0)
@@ -232,9 +235,12 @@ int launch_on_workspace(int group_count, const GroupArgs *args, long long total_
         const long long tiles = (long long)((a.m + kBlockM - 1) / kBlockM) * ((a.n + block_n - 1) / block_n);
         const long long kt = (a.k + kBlockK - 1) / kBlockK;
         total_work += tiles * (kt > 1 ? kt : 1);
+        if (a.k > 0)
+            ++desc_groups;
     }
     if (total_work > 0x7fffffffLL)
         return fail(NVFP4_ERR_UNSUPPORTED, "more than 2^31 - 1 k-tiles in one call");
+    DeviceState *st = nullptr;
     GemmLaunch cfg;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
@@ -242,25 +248,35 @@ int launch_on_workspace(int group_count, const GroupArgs *args, long long total_
         if (s != NVFP4_OK)
             return s;
         const int sms = st->sm_count;
-        cfg.split = (epoch != nullptr && partial_slots >= sms && want_split(total_tiles, sms)) ? 1 : 0;
+        cfg.split = (partial_slots >= sms && want_split(total_tiles, sms)) ? 1 : 0;
         if (cfg.split) {
             cfg.grid = (int)(total_work < sms ? total_work : sms);
-            cfg.epoch = ++*epoch;
+            cfg.epoch = ++state->epoch;
         } else {
             cfg.grid = (int)(total_tiles < sms ? total_tiles : sms);
             cfg.epoch = 0;
         }
+        if (group_count > kMediumGroups && prefix_slots < cfg.grid)
+            return fail(NVFP4_ERR_UNSUPPORTED, "workspace has %d CTA slots, the launch needs %d", prefix_slots,
+                        cfg.grid);
+        cfg.desc_base = state->desc_count;
+        state->desc_count += (uint32_t)desc_groups;
     }
     cfg.block_n = block_n;
     cfg.group_count = group_count;
+    cfg.desc_groups = desc_groups;
     cfg.total_tiles = (int)total_tiles;
     cfg.total_work = (int)total_work;
     cfg.timeout_ns = watchdog_ns();
-    const WorkspaceView ws = workspace_view(ws_base, capacity, partial_slots);
+    const WorkspaceView ws = workspace_view(ws_base, capacity, prefix_slots, partial_slots);
     const void *tmpl_b = block_n == 256 ? (const void *)&st->tmpl_b256 : (const void *)&st->tmpl_b128;
     e = launch_grouped(cfg, args, ws, &st->tmpl_a, tmpl_b, stream);
-    if (e != cudaSuccess)
+    if (e != cudaSuccess) {
+        // nothing ran: the device counter did not move
+        std::lock_guard<std::mutex> lock(g_mutex);
+        state->desc_count -= (uint32_t)desc_groups;
         return cuda_fail(e, "grouped GEMM launch");
+    }
     return NVFP4_OK;
 }
 
@@ -322,8 +338,8 @@ int nvfp4_grouped_gemm(int group_count, const nvfp4_problem_size *problem_sizes,
         if (s != NVFP4_OK)
             return s;
     }
-    return launch_on_workspace(group_count, args, total, block_n, w->base, NVFP4_MAX_GROUPS, w->partial_slots,
-                               &w->epoch, reinterpret_cast<cudaStream_t>(stream));
+    return launch_on_workspace(group_count, args, total, block_n, w->base, NVFP4_MAX_GROUPS, w->slots, w->slots,
+                               &w->state, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int nvfp4_pack_scales(const void *sf_rowmajor, int rows, int k, void *sf_atoms, nvfp4_stream_t stream) {

@@ -1,17 +1,19 @@
 // gemm.cu -- the grouped NVFP4 block-scaled GEMM for sm_103a.
 //
-// Two kernels per call, in stream order:
-//
-//  1. prologue_kernel (one CTA): per-group output-tile counts and schedule-unit
-//     counts with their exclusive prefix sums, a compact per-group table, and
-//     per-group TMA descriptors for A and B patched from a host-encoded
-//     template with tensormap.replace (the per-group descriptor patching of
-//     "nvfp4 group gemm" submission 506336, TMA warp, and the one-off descriptor
-//     initialisation kernel of submission 499344; here the tile prefix sum also
-//     moves to the device). It triggers programmatic dependent launch at once so
-//     the GEMM kernel's set-up overlaps it.
-//
-//  2. grouped_gemm_kernel<BN> (persistent, one CTA per SM, 320 threads):
+// One persistent kernel per call, grouped_gemm_kernel<BN, CAP> (one CTA per
+// SM, 320 threads, cooperative launch so every CTA is resident). The group
+// table (sizes and pointers of up to CAP groups) arrives as a __grid_constant__
+// kernel parameter, and at start-up every CTA
+//   * computes the per-group output-tile counts and schedule-unit counts and
+//     their exclusive prefix sums (one warp scan; the tile prefix sum that the
+//     "nvfp4 group gemm" submissions build on the host is built here), and
+//   * patches the TMA descriptors of its share of the groups (group g by CTA
+//     g mod gridDim) from a host-encoded template with tensormap.replace,
+//     releases them and bumps a publication counter; producers wait for the
+//     counter before their first copy (the per-group descriptor patching of
+//     submission 506336, TMA warp, and the descriptor initialisation kernel of
+//     submission 499344, done inside the one launch).
+// Roles:
 //       warp 4    TMA producer: A and B tiles (128-byte swizzle) plus the scale
 //                 runs of each 256-K k-tile (1-D bulk copies: a 128-row x 256-K
 //                 slice of the reordered scale layout is 4 consecutive 512-byte
@@ -25,21 +27,24 @@
 //                 128 x BN x 64, four per k-tile, into a TMEM accumulator;
 //                 commits free the smem stage and publish the accumulator;
 //       warps 0-3 epilogue: tcgen05.ld of the accumulator lanes they own,
-//                 fp32 -> fp16 round-to-nearest-even, 16-byte stores, rows
-//                 >= m skipped, column chunks >= n skipped.
+//                 fp32 -> fp16 round-to-nearest-even, staged through a
+//                 swizzled per-warp buffer so each store writes 8 rows x 64 B;
+//                 rows >= m and column chunks >= n skipped.
 //
 // Schedule. The work of a call is a sequence of schedule units: for every
 // output tile (group-major, M fastest inside a group, so neighbouring units
 // share a B panel) its k-tiles, at least one per tile (a k == 0 tile has one
-// unit and produces zeros). Each CTA takes one contiguous range of units:
-//   * whole-tile ranges (tiles split evenly over the CTAs) when there are many
-//     tiles per SM;
-//   * equal ranges of units (stream-K) when there are few: a tile may then be
-//     split along K between consecutive CTAs. The CTA holding the tile's first
-//     k-tile finishes it; every later piece is the first segment of its CTA,
-//     so it is computed without waiting, stored as an fp32 partial tile in the
-//     CTA's workspace slot and published with an epoch flag (release); the
-//     finishing CTA acquires the flags, adds the partials and writes C.
+// unit and produces zeros). CTAs take
+//   * whole tiles round-robin (tile blockIdx.x, + gridDim.x, ...) when there
+//     are many tiles per SM, so the CTAs running at one time work on
+//     neighbouring tiles and share their A and B panels in L2;
+//   * equal contiguous ranges of units (stream-K) when there are few: a tile
+//     may then be split along K between consecutive CTAs. The CTA holding the
+//     tile's first k-tile finishes it; every later piece is the first segment
+//     of its CTA, so it is computed without waiting, stored as an fp32 partial
+//     tile in the CTA's workspace slot and published with an epoch flag
+//     (release); the finishing CTA acquires the flags, adds the partials and
+//     writes C.
 //
 // Every wait is bounded (%globaltimer): a wait that gives up sets a bit in
 // the workspace status word and a CTA-wide abort flag, the other roles leave
@@ -55,9 +60,7 @@
 namespace nvfp4 {
 namespace {
 
-constexpr uint32_t kStatusFlagTimeout = 8u;
-
-template <int BN>
+template <int BN, int CAP>
 struct Cfg {
     static_assert(BN == 128 || BN == 256, "BLOCK_N");
     static constexpr int kStages = (BN == 128) ? 6 : 4;
@@ -80,13 +83,58 @@ struct Cfg {
     static constexpr int kThreads = 320;                           // 10 warps
     static constexpr int kBarrierBytes = 256;
     static_assert((3 * kStages + 2 * kAccStages) * 8 <= 192, "barrier area");
+    static constexpr int kEpiStageBytes = 32 * 64;                 // per epilogue warp: 32 rows x 32 fp16
+    // Prefix sums live in shared memory for up to kMediumGroups groups, else
+    // in the CTA's global scratch slot.
+    static constexpr bool kSmemPrefix = CAP <= kMediumGroups;
+    static constexpr int kPrefixInts = (int)round_up(CAP + 1, 4);
+    static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kBarrierBytes + 4 * kEpiStageBytes +
+                                         (kSmemPrefix ? 2 * sizeof(int32_t) * kPrefixInts : 0);
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
     static constexpr uint32_t kIdesc = ptx::idesc_mxf4nvf4(kBlockM, BN);
-
-    static size_t smem_bytes(int capacity) {
-        return 1024 + (size_t)kStages * kStageBytes + kBarrierBytes +
-               2 * round_up(sizeof(int32_t) * (capacity + 1), 16);
-    }
 };
+
+template <int CAP>
+struct GemmParams {
+    alignas(64) uint8_t tmpl_a[128];
+    alignas(64) uint8_t tmpl_b[128];
+    WorkspaceView ws;
+    int32_t group_count, block_n, total_tiles, total_work, split, desc_groups;
+    uint32_t epoch, desc_base;
+    uint64_t timeout_ns;
+    GroupArgs groups[CAP];
+};
+
+__device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+// Derived sizes of one group (m, n, k >= 0).
+struct GInfo {
+    int m, n, k;
+    int tiles_m, tiles;       // ceil(m / 128), ceil(m / 128) * ceil(n / BN) (0 for an empty group)
+    int k_tiles, k_blocks;    // ceil(k / 256), ceil(k / 64)
+    int work_tiles;           // max(k_tiles, 1): schedule units per output tile
+    int sf_row_blocks_b;      // ceil(n / 128): 128-row scale blocks of B
+    const uint8_t *sfa, *sfb;
+    void *c;
+};
+
+template <int BN>
+__device__ __forceinline__ GInfo group_info(const GroupArgs &a) {
+    GInfo g;
+    g.m = a.m;
+    g.n = a.n;
+    g.k = a.k;
+    g.tiles_m = ceil_div_i(a.m, kBlockM);
+    g.tiles = (a.m > 0 && a.n > 0) ? g.tiles_m * ceil_div_i(a.n, BN) : 0;
+    g.k_tiles = ceil_div_i(a.k, kBlockK);
+    g.k_blocks = ceil_div_i(a.k, kMmaK);
+    g.work_tiles = g.k_tiles > 1 ? g.k_tiles : 1;
+    g.sf_row_blocks_b = ceil_div_i(a.n, 128);
+    g.sfa = static_cast<const uint8_t *>(a.sfa);
+    g.sfb = static_cast<const uint8_t *>(a.sfb);
+    g.c = a.c;
+    return g;
+}
 
 // Index g with prefix[g] <= x < prefix[g + 1] (groups with no entries skipped).
 __device__ __forceinline__ int find_group(const int32_t *prefix, int group_count, int x) {
@@ -122,6 +170,22 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     }
 }
 
+// Wait until the global counter reaches `target` (modulo 2^32), acquire.
+__device__ __forceinline__ bool wait_counter(const uint32_t *counter, uint32_t target, volatile int *abort_flag,
+                                             uint64_t timeout_ns, uint32_t *status) {
+    const uint64_t t0 = ptx::globaltimer();
+    while ((int32_t)(ptx::ld_acquire_gpu(counter) - target) < 0) {
+        if (*abort_flag)
+            return false;
+        if (ptx::globaltimer() - t0 > timeout_ns) {
+            *abort_flag = 1;
+            atomicOr(status, kStatusDescTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
 // A run of one tile's k-tiles [kt0, kt1) (out of ktg schedule units) that one
 // CTA processes.
 struct Segment {
@@ -130,39 +194,63 @@ struct Segment {
     int w_tile_end;  // schedule index one past the tile's last unit
 };
 
-__device__ __forceinline__ Segment segment_at(int w, int w_end, const int32_t *wprefix, int group_count,
-                                              const GroupInfo *groups) {
-    Segment s;
-    s.g = find_group(wprefix, group_count, w);
-    const int ktg = groups[s.g].work_tiles;
-    const int local = w - wprefix[s.g];
-    const int t = local / ktg;
-    s.kt0 = local - t * ktg;
-    const int rest = w_end - w;
-    s.kt1 = s.kt0 + ((ktg - s.kt0) < rest ? (ktg - s.kt0) : rest);
-    s.ktg = ktg;
-    const int tiles_m = groups[s.g].tiles_m;
-    s.tm = t % tiles_m;
-    s.tn = t / tiles_m;
-    s.w_tile_end = wprefix[s.g] + (t + 1) * ktg;
-    return s;
-}
-
 // First schedule unit of CTA c out of p in a split (stream-K) schedule.
 __device__ __forceinline__ int split_begin(int c, int p, int total_work) {
     return (int)(((long long)c * total_work) / p);
 }
 
+// The sequence of segments one CTA processes; every role walks the same one.
 template <int BN>
-__global__ void __launch_bounds__(320, 1)
-    grouped_gemm_kernel(const WorkspaceView ws, const int group_count, const int total_tiles, const int total_work,
-                        const int split, const uint32_t epoch, const uint64_t timeout_ns) {
-    using C = Cfg<BN>;
+struct Cursor {
+    const int32_t *prefix, *wprefix;
+    const GroupArgs *groups;
+    int group_count, split;
+    int w, w_end;                 // split schedule: contiguous schedule units
+    int tile, total_tiles, step;  // whole-tile schedule: round-robin tiles
+
+    __device__ __forceinline__ bool next(Segment &s) {
+        int t;
+        if (split) {
+            if (w >= w_end)
+                return false;
+            s.g = find_group(wprefix, group_count, w);
+            const GInfo gi = group_info<BN>(groups[s.g]);
+            const int local = w - wprefix[s.g];
+            t = local / gi.work_tiles;
+            s.ktg = gi.work_tiles;
+            s.kt0 = local - t * gi.work_tiles;
+            const int rest = w_end - w;
+            s.kt1 = s.kt0 + ((s.ktg - s.kt0) < rest ? (s.ktg - s.kt0) : rest);
+            s.tm = t % gi.tiles_m;
+            s.tn = t / gi.tiles_m;
+            w += s.kt1 - s.kt0;
+        } else {
+            if (tile >= total_tiles)
+                return false;
+            s.g = find_group(prefix, group_count, tile);
+            const GInfo gi = group_info<BN>(groups[s.g]);
+            t = tile - prefix[s.g];
+            s.tm = t % gi.tiles_m;
+            s.tn = t / gi.tiles_m;
+            s.ktg = gi.work_tiles;
+            s.kt0 = 0;
+            s.kt1 = s.ktg;
+            tile += step;
+        }
+        s.w_tile_end = wprefix[s.g] + (t + 1) * s.ktg;
+        return true;
+    }
+};
+
+template <int BN, int CAP>
+__global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams<CAP> p) {
+    using C = Cfg<BN, CAP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t smem_base = ptx::smem_addr(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int group_count = p.group_count;
 
     uint8_t *bar_area = smem + C::kStages * C::kStageBytes;
     const uint32_t bars = ptx::smem_addr(bar_area);
@@ -173,62 +261,104 @@ __global__ void __launch_bounds__(320, 1)
     auto acce_bar = [&](int a) { return bars + 8u * (3 * C::kStages + C::kAccStages + a); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_area + 192);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 196);
-    int *s_range = reinterpret_cast<int *>(bar_area + 200);           // [w_begin, w_end)
     volatile int *s_epi_ok = reinterpret_cast<volatile int *>(bar_area + 208);
-    const size_t prefix_bytes = round_up(sizeof(int32_t) * (group_count + 1), 16);
-    int32_t *s_prefix = reinterpret_cast<int32_t *>(bar_area + C::kBarrierBytes);
-    int32_t *s_wprefix = reinterpret_cast<int32_t *>(bar_area + C::kBarrierBytes + prefix_bytes);
+    uint8_t *epi_stage = bar_area + C::kBarrierBytes;                // [4 warps][32 rows][64 B]
+    int32_t *prefix;
+    if constexpr (C::kSmemPrefix)
+        prefix = reinterpret_cast<int32_t *>(epi_stage + 4 * C::kEpiStageBytes);
+    else
+        prefix = p.ws.cta_prefix + (size_t)blockIdx.x * (cta_prefix_bytes(CAP) / sizeof(int32_t));
+    int32_t *wprefix = prefix + (C::kSmemPrefix ? C::kPrefixInts : (int)(cta_prefix_bytes(CAP) / 8));
 
-    // ---- set-up that does not depend on the prologue -----------------------
-    if (warp == 4 && lane == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            ptx::mbar_init(full_bar(s), 1);
-            ptx::mbar_init(empty_bar(s), 1);
-            ptx::mbar_init(sff_bar(s), 4);
+    // ---- set-up -------------------------------------------------------------
+    if (warp == 4) {
+        if (lane == 0) {
+            for (int s = 0; s < C::kStages; ++s) {
+                ptx::mbar_init(full_bar(s), 1);
+                ptx::mbar_init(empty_bar(s), 1);
+                ptx::mbar_init(sff_bar(s), 4);
+            }
+            for (int a = 0; a < C::kAccStages; ++a) {
+                ptx::mbar_init(accf_bar(a), 1);
+                ptx::mbar_init(acce_bar(a), 4);
+            }
+            *abort_flag = 0;
+            ptx::fence_mbar_init();
         }
-        for (int a = 0; a < C::kAccStages; ++a) {
-            ptx::mbar_init(accf_bar(a), 1);
-            ptx::mbar_init(acce_bar(a), 4);
+        // Patch the descriptors of this CTA's share of the groups.
+        uint32_t patched = 0;
+        for (int g = blockIdx.x + lane * gridDim.x; g < group_count; g += 32 * gridDim.x) {
+            const GroupArgs &a = p.groups[g];
+            if (a.m <= 0 || a.n <= 0 || a.k <= 0)
+                continue;
+            uint8_t *ta = p.ws.tmaps + (size_t)g * 2 * kDescBytes;
+            uint8_t *tb = ta + kDescBytes;
+            const uint4 *src_a = reinterpret_cast<const uint4 *>(p.tmpl_a);
+            const uint4 *src_b = reinterpret_cast<const uint4 *>(p.tmpl_b);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                reinterpret_cast<uint4 *>(ta)[q] = src_a[q];
+                reinterpret_cast<uint4 *>(tb)[q] = src_b[q];
+            }
+            const uint32_t row_bytes = (uint32_t)(a.k / 2);
+            ptx::tmap_set_address(ta, a.a);
+            ptx::tmap_set_dims(ta, row_bytes, (uint32_t)a.m);
+            ptx::tmap_set_stride1(ta, row_bytes);
+            ptx::tmap_set_address(tb, a.b);
+            ptx::tmap_set_dims(tb, row_bytes, (uint32_t)a.n);
+            ptx::tmap_set_stride1(tb, row_bytes);
+            ++patched;
         }
-        *abort_flag = 0;
-        ptx::fence_mbar_init();
-    }
-    if (warp == 5) {
+        if (patched) {
+            ptx::tmap_release();
+            ptx::red_release_add_gpu(p.ws.desc_count, patched);
+        }
+    } else if (warp == 5) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::kTmemCols);
         ptx::tmem_relinquish();
-    }
-
-    // ---- wait for the prologue's prefix sums, group table and descriptors --
-    ptx::griddep_wait();
-    for (int i = threadIdx.x; i <= group_count; i += blockDim.x) {
-        s_prefix[i] = ws.prefix[i];
-        s_wprefix[i] = ws.wprefix[i];
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const int c = blockIdx.x, p = gridDim.x;
-        if (split) {
-            s_range[0] = split_begin(c, p, total_work);
-            s_range[1] = split_begin(c + 1, p, total_work);
-        } else {
-            // whole tiles: [c*T/p, (c+1)*T/p) mapped to schedule units
-            for (int e = 0; e < 2; ++e) {
-                const int t = (int)(((long long)(c + e) * total_tiles) / p);
-                if (t >= total_tiles) {
-                    s_range[e] = total_work;
-                } else {
-                    const int g = find_group(s_prefix, group_count, t);
-                    s_range[e] = s_wprefix[g] + (t - s_prefix[g]) * ws.groups[g].work_tiles;
-                }
+    } else if (warp == 6) {
+        // Exclusive prefix sums of output tiles and schedule units per group:
+        // lane l takes a contiguous run of groups, then one warp scan.
+        const int per = (group_count + 31) / 32;
+        const int g0 = lane * per;
+        const int g1 = (g0 + per) < group_count ? (g0 + per) : group_count;
+        int st = 0, sw = 0;
+        for (int g = g0; g < g1; ++g) {
+            const GInfo gi = group_info<BN>(p.groups[g]);
+            st += gi.tiles;
+            sw += gi.tiles * gi.work_tiles;
+        }
+        int it = st, iw = sw;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int yt = __shfl_up_sync(0xffffffffu, it, off);
+            const int yw = __shfl_up_sync(0xffffffffu, iw, off);
+            if (lane >= off) {
+                it += yt;
+                iw += yw;
             }
+        }
+        int bt = it - st, bw = iw - sw;
+        for (int g = g0; g < g1; ++g) {
+            const GInfo gi = group_info<BN>(p.groups[g]);
+            prefix[g] = bt;
+            wprefix[g] = bw;
+            bt += gi.tiles;
+            bw += gi.tiles * gi.work_tiles;
+        }
+        if (lane == 31) {
+            prefix[group_count] = it;
+            wprefix[group_count] = iw;
         }
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int w_begin = s_range[0];
-    const int w_end = s_range[1];
+    const Cursor<BN> cursor0{prefix, wprefix, p.groups, group_count, p.split,
+                             split_begin(blockIdx.x, gridDim.x, p.total_work),
+                             split_begin(blockIdx.x + 1, gridDim.x, p.total_work),
+                             (int)blockIdx.x, p.total_tiles, (int)gridDim.x};
 
     if (warp == 4) {
         // ===================== TMA producer =====================
@@ -239,18 +369,28 @@ __global__ void __launch_bounds__(320, 1)
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
             int prev_g = -1;
+            bool descs_ready = p.desc_groups == 0;
             bool ok = true;
-            for (int w = w_begin; ok && w < w_end;) {
-                const Segment sg = segment_at(w, w_end, s_wprefix, group_count, ws.groups);
-                w += sg.kt1 - sg.kt0;
-                const GroupInfo &gi = ws.groups[sg.g];
+            Cursor<BN> cur = cursor0;
+            Segment sg;
+            while (ok && cur.next(sg)) {
+                const GInfo gi = group_info<BN>(p.groups[sg.g]);
                 const int k_tiles = gi.k_tiles;
                 const int kend = sg.kt1 < k_tiles ? sg.kt1 : k_tiles;
                 if (sg.kt0 >= kend)
                     continue;  // k == 0 tile: nothing to load
                 const int k_blocks = gi.k_blocks;
-                const uint8_t *tmap_a = ws.tmaps + (size_t)sg.g * 256;
+                const uint8_t *tmap_a = p.ws.tmaps + (size_t)sg.g * 256;
                 const uint8_t *tmap_b = tmap_a + 128;
+                if (!descs_ready) {
+                    // every group's descriptors are patched by some CTA at start-up
+                    if (!wait_counter(p.ws.desc_count, p.desc_base + (uint32_t)p.desc_groups, abort_flag,
+                                      p.timeout_ns, p.ws.status)) {
+                        ok = false;
+                        break;
+                    }
+                    descs_ready = true;
+                }
                 if (sg.g != prev_g) {
                     ptx::tmap_acquire(tmap_a);
                     ptx::tmap_acquire(tmap_b);
@@ -261,7 +401,7 @@ __global__ void __launch_bounds__(320, 1)
                 sfb_blocks = sfb_blocks < C::kSfbRowBlocks ? sfb_blocks : C::kSfbRowBlocks;
                 const uint8_t *sfb = gi.sfb + (size_t)sg.tn * C::kSfbRowBlocks * k_blocks * kSfAtomBytes;
                 for (int kt = sg.kt0; kt < kend; ++kt) {
-                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, timeout_ns, ws.status,
+                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns, p.ws.status,
                                       kStatusProducerTimeout)) {
                         ok = false;
                         break;
@@ -293,7 +433,7 @@ __global__ void __launch_bounds__(320, 1)
                         continue;
                     const uint32_t par = (armed_parity >> s) & 1u;
                     const uint64_t t0 = ptx::globaltimer();
-                    while (!ptx::mbar_try_wait(full_bar(s), par) && ptx::globaltimer() - t0 < timeout_ns) {
+                    while (!ptx::mbar_try_wait(full_bar(s), par) && ptx::globaltimer() - t0 < p.timeout_ns) {
                     }
                 }
             }
@@ -304,21 +444,22 @@ __global__ void __launch_bounds__(320, 1)
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int w = w_begin; ok && w < w_end;) {
-                const Segment sg = segment_at(w, w_end, s_wprefix, group_count, ws.groups);
-                w += sg.kt1 - sg.kt0;
-                const int k_tiles = ws.groups[sg.g].k_tiles;
-                const int k_blocks = ws.groups[sg.g].k_blocks;
+            Cursor<BN> cur = cursor0;
+            Segment sg;
+            while (ok && cur.next(sg)) {
+                const GInfo gi = group_info<BN>(p.groups[sg.g]);
+                const int k_tiles = gi.k_tiles;
+                const int k_blocks = gi.k_blocks;
                 const int kend = sg.kt1 < k_tiles ? sg.kt1 : k_tiles;
-                if (!wait_bounded(acce_bar(acc), acc_phase ^ 1u, abort_flag, timeout_ns, ws.status,
+                if (!wait_bounded(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns, p.ws.status,
                                   kStatusMmaTimeout))
                     break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::kAccCols);
                 for (int kt = sg.kt0; kt < kend; ++kt) {
-                    if (!wait_bounded(full_bar(stage), phase, abort_flag, timeout_ns, ws.status,
+                    if (!wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status,
                                       kStatusMmaTimeout) ||
-                        !wait_bounded(sff_bar(stage), phase, abort_flag, timeout_ns, ws.status,
+                        !wait_bounded(sff_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status,
                                       kStatusMmaTimeout)) {
                         ok = false;
                         break;
@@ -358,16 +499,17 @@ __global__ void __launch_bounds__(320, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int w = w_begin; ok && w < w_end;) {
-            const Segment sg = segment_at(w, w_end, s_wprefix, group_count, ws.groups);
-            w += sg.kt1 - sg.kt0;
-            const int k_tiles = ws.groups[sg.g].k_tiles;
-            const int k_blocks = ws.groups[sg.g].k_blocks;
+        Cursor<BN> cur = cursor0;
+        Segment sg;
+        while (ok && cur.next(sg)) {
+            const GInfo gi = group_info<BN>(p.groups[sg.g]);
+            const int k_tiles = gi.k_tiles;
+            const int k_blocks = gi.k_blocks;
             const int kend = sg.kt1 < k_tiles ? sg.kt1 : k_tiles;
             for (int kt = sg.kt0; kt < kend; ++kt) {
                 int got = 0;
                 if (lane == 0)
-                    got = wait_bounded(full_bar(stage), phase, abort_flag, timeout_ns, ws.status, kStatusMmaTimeout)
+                    got = wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status, kStatusMmaTimeout)
                               ? 1
                               : 0;
                 got = __shfl_sync(0xffffffffu, got, 0);
@@ -407,29 +549,29 @@ __global__ void __launch_bounds__(320, 1)
         const int r_local = warp * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int w = w_begin; w < w_end;) {
-            const Segment sg = segment_at(w, w_end, s_wprefix, group_count, ws.groups);
-            w += sg.kt1 - sg.kt0;
-            const GroupInfo &gi = ws.groups[sg.g];
+        Cursor<BN> cur = cursor0;
+        Segment sg;
+        while (cur.next(sg)) {
+            const GInfo gi = group_info<BN>(p.groups[sg.g]);
             const int m = gi.m, n = gi.n;
             const bool zero = gi.k == 0;
             const bool cont = sg.kt0 > 0;                                       // a later piece of a split tile
-            const bool finish_split = split && sg.kt0 == 0 && sg.kt1 < sg.ktg;  // first piece of a split tile
+            const bool finish_split = p.split && sg.kt0 == 0 && sg.kt1 < sg.ktg;  // first piece of a split tile
             // One thread waits (for the accumulator and, when finishing a split
             // tile, for the later pieces' flags); the four warps leave or stay
             // together: the TMEM loads below are warp-collective.
             if (threadIdx.x == 0) {
-                int ok = wait_bounded(accf_bar(acc), acc_phase, abort_flag, timeout_ns, ws.status,
+                int ok = wait_bounded(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns, p.ws.status,
                                       kStatusEpilogueTimeout)
                              ? 1
                              : 0;
                 if (ok && finish_split) {
-                    for (int c2 = cta + 1; c2 < ncta && split_begin(c2, ncta, total_work) < sg.w_tile_end; ++c2) {
+                    for (int c2 = cta + 1; c2 < ncta && split_begin(c2, ncta, p.total_work) < sg.w_tile_end; ++c2) {
                         const uint64_t t0 = ptx::globaltimer();
-                        while (ptx::ld_acquire_gpu(ws.flags + c2) != epoch) {
-                            if (ptx::globaltimer() - t0 > timeout_ns) {
+                        while (ptx::ld_acquire_gpu(p.ws.flags + c2) != p.epoch) {
+                            if (ptx::globaltimer() - t0 > p.timeout_ns) {
                                 *abort_flag = 1;
-                                atomicOr(ws.status, kStatusFlagTimeout);
+                                atomicOr(p.ws.status, kStatusFlagTimeout);
                                 ok = 0;
                                 break;
                             }
@@ -446,38 +588,68 @@ __global__ void __launch_bounds__(320, 1)
             ptx::tc_fence_after();
             const int row = sg.tm * kBlockM + r_local;
             const uint32_t t_row = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * C::kAccCols);
-            __half *c_row = static_cast<__half *>(gi.c) + (size_t)row * (size_t)n;
+            __half *c_base = static_cast<__half *>(gi.c);
+            uint8_t *buf = epi_stage + warp * C::kEpiStageBytes;
+            // Partial tiles: [chunk][quad q][row] of float4, so a warp's stores
+            // and loads of one (chunk, q) cover 512 contiguous bytes. When
+            // finishing a split tile, the first later piece's next chunk is
+            // loaded while the current one is converted (L2 latency hidden).
+            const int nchunks = (n - sg.tn * BN) / 32 < BN / 32 ? (n - sg.tn * BN) / 32 : BN / 32;
+            const bool prefetch = finish_split && row < m;
+            float4 pf[8];
+            if (prefetch) {
+                const float4 *src = reinterpret_cast<const float4 *>(p.ws.partials) +
+                                    (size_t)(cta + 1) * (kPartialSlotBytes / 16) + r_local;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    pf[q] = __ldcg(src + q * kBlockM);
+            }
 #pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
+            for (int cc = 0; cc < nchunks; ++cc) {
                 const int col = sg.tn * BN + cc * 32;
-                if (col >= n)
-                    break;
                 uint32_t v[32];
                 ptx::tmem_ld_32x32b_x32(t_row + cc * 32, v);
                 ptx::tmem_ld_wait();
-                if (row >= m)
-                    continue;
-                const size_t part_off = ((size_t)cc * kBlockM + r_local) * 32;
+                float4 *part = reinterpret_cast<float4 *>(p.ws.partials) + ((size_t)cc * 8) * kBlockM + r_local;
                 if (cont) {
-                    float4 *dst = reinterpret_cast<float4 *>(ws.partials + (size_t)cta * (kPartialSlotBytes / 4) +
-                                                             part_off);
+                    if (row < m) {
+                        float4 *dst = part + (size_t)cta * (kPartialSlotBytes / 16);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                             __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                        for (int q = 0; q < 8; ++q)
+                            dst[q * kBlockM] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                           __uint_as_float(v[4 * q + 2]),
+                                                           __uint_as_float(v[4 * q + 3]));
+                    }
                     continue;
                 }
                 float f[32];
 #pragma unroll
                 for (int q = 0; q < 32; ++q)
                     f[q] = zero ? 0.0f : __uint_as_float(v[q]);
-                if (finish_split) {
-                    for (int c2 = cta + 1; c2 < ncta && split_begin(c2, ncta, total_work) < sg.w_tile_end; ++c2) {
-                        const float4 *src = reinterpret_cast<const float4 *>(
-                            ws.partials + (size_t)c2 * (kPartialSlotBytes / 4) + part_off);
+                if (prefetch) {
+                    float4 cur[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        cur[q] = pf[q];
+                    if (cc + 1 < nchunks) {
+                        const float4 *src = part + 8 * kBlockM + (size_t)(cta + 1) * (kPartialSlotBytes / 16);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            pf[q] = __ldcg(src + q * kBlockM);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        f[4 * q] += cur[q].x;
+                        f[4 * q + 1] += cur[q].y;
+                        f[4 * q + 2] += cur[q].z;
+                        f[4 * q + 3] += cur[q].w;
+                    }
+                    // further pieces of the same tile (rare: a tile spanning 3+ CTAs)
+                    for (int c2 = cta + 2; c2 < ncta && split_begin(c2, ncta, p.total_work) < sg.w_tile_end; ++c2) {
+                        const float4 *src = part + (size_t)c2 * (kPartialSlotBytes / 16);
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
-                            const float4 p4 = __ldcg(src + q);
+                            const float4 p4 = __ldcg(src + q * kBlockM);
                             f[4 * q] += p4.x;
                             f[4 * q + 1] += p4.y;
                             f[4 * q + 2] += p4.z;
@@ -485,16 +657,32 @@ __global__ void __launch_bounds__(320, 1)
                         }
                     }
                 }
+                // fp16 row segment (64 B) -> this warp's staging buffer, 16-byte
+                // pieces XOR-swizzled by (row / 2) % 4 so that neither the
+                // row-wise writes nor the transposed reads conflict on banks.
                 uint32_t h[16];
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
                     __half2 p2 = __floats2half2_rn(f[2 * q], f[2 * q + 1]);
                     h[q] = *reinterpret_cast<uint32_t *>(&p2);
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(c_row + col);
+                const int sw = (lane >> 1) & 3;
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    dst[q] = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4 *>(buf + lane * 64 + 16 * (j ^ sw)) =
+                        make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+                __syncwarp();
+                // 4 lanes per row: each store instruction writes 8 rows x 64 B.
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int r = 8 * q + (lane >> 2);
+                    const int piece = lane & 3;
+                    const uint4 val = *reinterpret_cast<const uint4 *>(buf + r * 64 + 16 * (piece ^ ((r >> 1) & 3)));
+                    const int grow = sg.tm * kBlockM + warp * 32 + r;
+                    if (grow < m)
+                        *reinterpret_cast<uint4 *>(c_base + (size_t)grow * (size_t)n + col + 8 * piece) = val;
+                }
+                __syncwarp();
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -505,7 +693,7 @@ __global__ void __launch_bounds__(320, 1)
                 ptx::named_barrier(1, 128);
                 if (threadIdx.x == 0) {
                     __threadfence();
-                    ptx::st_release_gpu(ws.flags + cta, epoch);
+                    ptx::st_release_gpu(p.ws.flags + cta, p.epoch);
                 }
             }
             if (++acc == C::kAccStages) {
@@ -524,168 +712,55 @@ __global__ void __launch_bounds__(320, 1)
     }
 }
 
-// ---------------------------------------------------------------------------
-// Prologue: tile and schedule-unit counts, prefix sums, group table, per-group
-// TMA descriptors.
-
-template <int CAP>
-struct PrologueParams {
-    alignas(64) uint8_t tmpl_a[128];
-    alignas(64) uint8_t tmpl_b[128];
-    WorkspaceView ws;
-    int32_t group_count;
-    int32_t block_n;
-    GroupArgs groups[CAP];
-};
-
-__device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
-
-// Exclusive prefix sum over the block (blockDim.x <= 1024); returns this
-// thread's exclusive value and writes the block total to *total.
-__device__ __forceinline__ int block_exclusive_scan(int x, int32_t *warp_sums, int *total) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nwarps = (blockDim.x + 31) >> 5;
-    int v = x;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, v, off);
-        if (lane >= off)
-            v += y;
-    }
-    if (lane == 31)
-        warp_sums[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-        int s = lane < nwarps ? warp_sums[lane] : 0;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, s, off);
-            if (lane >= off)
-                s += y;
-        }
-        warp_sums[lane] = s;
-    }
-    __syncthreads();
-    const int inclusive = v + (warp > 0 ? warp_sums[warp - 1] : 0);
-    *total = warp_sums[31];
-    __syncthreads();
-    return inclusive - x;
-}
-
-template <int CAP>
-__global__ void __launch_bounds__(CAP < 32 ? 32 : CAP)
-    prologue_kernel(const __grid_constant__ PrologueParams<CAP> p) {
-    // The GEMM kernel may start its set-up now; it waits for this grid's
-    // completion before it reads anything written here.
-    ptx::griddep_launch_dependents();
-    __shared__ int32_t warp_sums[32];
-    const int tid = threadIdx.x;
-    const int G = p.group_count;
-
-    int tiles = 0, work = 0;
-    if (tid < G) {
-        const GroupArgs &a = p.groups[tid];
-        if (a.m > 0 && a.n > 0) {
-            tiles = ceil_div_i(a.m, kBlockM) * ceil_div_i(a.n, p.block_n);
-            const int kt = ceil_div_i(a.k > 0 ? a.k : 0, kBlockK);
-            work = tiles * (kt > 1 ? kt : 1);
-        }
-    }
-    int total_tiles = 0, total_work = 0;
-    const int t_ex = block_exclusive_scan(tiles, warp_sums, &total_tiles);
-    const int w_ex = block_exclusive_scan(work, warp_sums, &total_work);
-    if (tid < G) {
-        p.ws.prefix[tid] = t_ex;
-        p.ws.wprefix[tid] = w_ex;
-    }
-    if (tid == 0) {
-        p.ws.prefix[G] = total_tiles;
-        p.ws.wprefix[G] = total_work;
-    }
-
-    if (tid < G) {
-        const GroupArgs &a = p.groups[tid];
-        GroupInfo gi;
-        gi.m = a.m;
-        gi.n = a.n;
-        gi.k = a.k;
-        gi.tiles_m = ceil_div_i(a.m > 0 ? a.m : 0, kBlockM);
-        gi.k_tiles = ceil_div_i(a.k > 0 ? a.k : 0, kBlockK);
-        gi.k_blocks = ceil_div_i(a.k > 0 ? a.k : 0, kMmaK);
-        gi.sf_row_blocks_b = ceil_div_i(a.n > 0 ? a.n : 0, 128);
-        gi.work_tiles = gi.k_tiles > 1 ? gi.k_tiles : 1;
-        gi.sfa = static_cast<const uint8_t *>(a.sfa);
-        gi.sfb = static_cast<const uint8_t *>(a.sfb);
-        gi.c = a.c;
-        gi.pad1 = 0;
-        p.ws.groups[tid] = gi;
-        if (a.m > 0 && a.n > 0 && a.k > 0) {
-            uint8_t *ta = p.ws.tmaps + (size_t)tid * 256;
-            uint8_t *tb = ta + 128;
-            const uint4 *src_a = reinterpret_cast<const uint4 *>(p.tmpl_a);
-            const uint4 *src_b = reinterpret_cast<const uint4 *>(p.tmpl_b);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                reinterpret_cast<uint4 *>(ta)[q] = src_a[q];
-                reinterpret_cast<uint4 *>(tb)[q] = src_b[q];
-            }
-            const uint32_t row_bytes = (uint32_t)(a.k / 2);
-            ptx::tmap_set_address(ta, a.a);
-            ptx::tmap_set_dims(ta, row_bytes, (uint32_t)a.m);
-            ptx::tmap_set_stride1(ta, row_bytes);
-            ptx::tmap_set_address(tb, a.b);
-            ptx::tmap_set_dims(tb, row_bytes, (uint32_t)a.n);
-            ptx::tmap_set_stride1(tb, row_bytes);
-            ptx::tmap_release();
-        }
-    }
-}
-
-template <int CAP>
-cudaError_t launch_prologue(const GemmLaunch &cfg, const GroupArgs *groups, const WorkspaceView &ws,
-                            const void *tmpl_a, const void *tmpl_b, cudaStream_t stream) {
-    PrologueParams<CAP> p;
-    std::memcpy(p.tmpl_a, tmpl_a, 128);
-    std::memcpy(p.tmpl_b, tmpl_b, 128);
-    p.ws = ws;
-    p.group_count = cfg.group_count;
-    p.block_n = cfg.block_n;
-    std::memcpy(p.groups, groups, sizeof(GroupArgs) * (size_t)cfg.group_count);
+template <int BN, int CAP>
+cudaError_t launch_cap(const GemmLaunch &cfg, const GroupArgs *groups, const WorkspaceView &ws,
+                       const void *tmpl_a, const void *tmpl_b, cudaStream_t stream) {
+    static_assert(sizeof(GemmParams<CAP>) <= 32000, "kernel parameter limit");
+    GemmParams<CAP> prm;
+    std::memcpy(prm.tmpl_a, tmpl_a, 128);
+    std::memcpy(prm.tmpl_b, tmpl_b, 128);
+    prm.ws = ws;
+    prm.group_count = cfg.group_count;
+    prm.block_n = cfg.block_n;
+    prm.total_tiles = cfg.total_tiles;
+    prm.total_work = cfg.total_work;
+    prm.split = cfg.split;
+    prm.desc_groups = cfg.desc_groups;
+    prm.epoch = cfg.epoch;
+    prm.desc_base = cfg.desc_base;
+    prm.timeout_ns = cfg.timeout_ns;
+    std::memcpy(prm.groups, groups, sizeof(GroupArgs) * (size_t)cfg.group_count);
     if (cfg.group_count < CAP)
-        std::memset(p.groups + cfg.group_count, 0, sizeof(GroupArgs) * (size_t)(CAP - cfg.group_count));
-    prologue_kernel<CAP><<<1, CAP < 32 ? 32 : CAP, 0, stream>>>(p);
-    return cudaGetLastError();
-}
-
-template <int BN>
-cudaError_t launch_main(const GemmLaunch &cfg, const WorkspaceView &ws, cudaStream_t stream) {
+        std::memset(prm.groups + cfg.group_count, 0, sizeof(GroupArgs) * (size_t)(CAP - cfg.group_count));
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)cfg.grid, 1, 1);
-    lc.blockDim = dim3(Cfg<BN>::kThreads, 1, 1);
-    lc.dynamicSmemBytes = Cfg<BN>::smem_bytes(ws.capacity);
+    lc.blockDim = dim3(Cfg<BN, CAP>::kThreads, 1, 1);
+    lc.dynamicSmemBytes = Cfg<BN, CAP>::kSmemBytes;
     lc.stream = stream;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    return cudaLaunchKernelEx(&lc, grouped_gemm_kernel<BN>, ws, cfg.group_count, cfg.total_tiles, cfg.total_work,
-                              cfg.split, cfg.epoch, cfg.timeout_ns);
+    return cudaLaunchKernelEx(&lc, grouped_gemm_kernel<BN, CAP>, prm);
 }
 
 }  // namespace
 
-size_t gemm_smem_bytes(int block_n) {
-    return block_n == 256 ? Cfg<256>::smem_bytes(NVFP4_MAX_GROUPS) : Cfg<128>::smem_bytes(NVFP4_MAX_GROUPS);
-}
-
 cudaError_t prepare_gemm_kernels(int /*device*/) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Cfg<128>::smem_bytes(NVFP4_MAX_GROUPS));
-    if (e != cudaSuccess)
-        return e;
-    return cudaFuncSetAttribute(grouped_gemm_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)Cfg<256>::smem_bytes(NVFP4_MAX_GROUPS));
+    cudaError_t e = cudaSuccess;
+#define NVFP4_SET_SMEM(BN, CAP)                                                                             \
+    if (e == cudaSuccess)                                                                                   \
+        e = cudaFuncSetAttribute(grouped_gemm_kernel<BN, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                 (int)Cfg<BN, CAP>::kSmemBytes);
+    NVFP4_SET_SMEM(128, kSmallGroups)
+    NVFP4_SET_SMEM(128, kMediumGroups)
+    NVFP4_SET_SMEM(128, NVFP4_MAX_GROUPS)
+    NVFP4_SET_SMEM(256, kSmallGroups)
+    NVFP4_SET_SMEM(256, kMediumGroups)
+    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS)
+#undef NVFP4_SET_SMEM
+    return e;
 }
 
 cudaError_t launch_grouped(const GemmLaunch &cfg, const GroupArgs *groups, const WorkspaceView &ws,
@@ -694,16 +769,17 @@ cudaError_t launch_grouped(const GemmLaunch &cfg, const GroupArgs *groups, const
         return cudaErrorInvalidValue;
     if (cfg.split && ws.partial_slots < cfg.grid)
         return cudaErrorInvalidValue;
-    cudaError_t e;
-    if (cfg.group_count <= 8)
-        e = launch_prologue<8>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
-    else if (cfg.group_count <= 64)
-        e = launch_prologue<64>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
-    else
-        e = launch_prologue<NVFP4_MAX_GROUPS>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
-    if (e != cudaSuccess)
-        return e;
-    return cfg.block_n == 256 ? launch_main<256>(cfg, ws, stream) : launch_main<128>(cfg, ws, stream);
+    if (cfg.group_count > kMediumGroups && ws.prefix_slots < cfg.grid)
+        return cudaErrorInvalidValue;
+    const bool wide = cfg.block_n == 256;
+    if (cfg.group_count <= kSmallGroups)
+        return wide ? launch_cap<256, kSmallGroups>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
+                    : launch_cap<128, kSmallGroups>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
+    if (cfg.group_count <= kMediumGroups)
+        return wide ? launch_cap<256, kMediumGroups>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
+                    : launch_cap<128, kMediumGroups>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
+    return wide ? launch_cap<256, NVFP4_MAX_GROUPS>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
+                : launch_cap<128, NVFP4_MAX_GROUPS>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
 }
 
 }  // namespace nvfp4

@@ -1,4 +1,5 @@
-// internal.h -- structures shared by the host layer (api.cu) and the kernels.
+// internal.h -- structures shared by the host layer (api.cu, noalloc.cu) and
+// the kernels (gemm.cu, pack_scales.cu).
 #pragma once
 
 #include <cstddef>
@@ -18,75 +19,69 @@ constexpr int kBlockK = 256;
 constexpr int kMmaK = 64;
 constexpr int kSfAtomBytes = 512;  // 128 rows x 4 scale blocks
 
-// One group as the prologue writes it for the GEMM kernel (64 bytes).
-struct GroupInfo {
-    int32_t m, n, k;
-    int32_t tiles_m;          // ceil(m / BLOCK_M)
-    int32_t k_tiles;          // ceil(k / BLOCK_K)
-    int32_t k_blocks;         // ceil(k / 64): MMA k-blocks = scale atoms along K
-    int32_t sf_row_blocks_b;  // ceil(n / 128): 128-row scale blocks that exist for B
-    int32_t work_tiles;       // max(k_tiles, 1): schedule units per output tile
-    const uint8_t *sfa;
-    const uint8_t *sfb;
-    void *c;
-    uint64_t pad1;
-};
-static_assert(sizeof(GroupInfo) == 64, "GroupInfo layout");
-
-// A group's raw arguments (host -> prologue, by kernel parameter).
+// A group's arguments, passed to the GEMM kernel as a kernel parameter.
 struct GroupArgs {
     int32_t m, n, k, l;
     const void *a, *b, *sfa, *sfb;
     void *c;
 };
 
-// Device workspace, carved from one allocation at 128-byte aligned offsets.
-//   status    uint32 (bit flags of bounded waits that gave up)
-//   prefix    int32 [capacity + 1]  exclusive prefix sum of output tiles per group
-//   wprefix   int32 [capacity + 1]  exclusive prefix sum of schedule units
-//                                   (tiles x max(k-tiles, 1)) per group
-//   groups    GroupInfo [capacity]
-//   tmaps     128-byte TMA descriptors [capacity][2] (A, B)
-//   flags     uint32 [slots]        epoch of the partial sum a CTA published
-//   partials  fp32 [slots][BLOCK_M x 256]  split-K partial tiles, one slot per CTA
-// The last two exist only when partial_slots > 0 (split schedules allowed).
-struct WorkspaceView {
-    uint32_t *status;
-    int32_t *prefix;
-    int32_t *wprefix;
-    GroupInfo *groups;
-    uint8_t *tmaps;
-    uint32_t *flags;
-    float *partials;
-    int32_t capacity;
-    int32_t partial_slots;
-};
+// Group counts with a kernel instantiation (the parameter block holds
+// GroupArgs[CAP]); calls use the smallest that fits.
+constexpr int kSmallGroups = 8;
+constexpr int kMediumGroups = 64;
 
 __host__ __device__ constexpr size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr size_t kPartialSlotBytes = sizeof(float) * 128 * 256;
+constexpr int kDescBytes = 128;
 
-constexpr size_t workspace_bytes(int capacity, int partial_slots = 0) {
-    return 128 + 2 * round_up(sizeof(int32_t) * (size_t)(capacity + 1), 128) +
-           round_up(sizeof(GroupInfo) * (size_t)capacity, 128) + 256 * (size_t)capacity +
+// Per-CTA prefix-sum scratch in global memory, used when the group count is
+// too large for the kernel's spare shared memory: [tiles prefix | units prefix].
+__host__ __device__ constexpr size_t cta_prefix_bytes(int capacity) { return 2 * round_up(sizeof(int32_t) * (size_t)(capacity + 1), 128); }
+
+// Device workspace, carved from one allocation at 128-byte aligned offsets.
+//   header      128 B: status word (bit flags of bounded waits that gave up) at
+//               byte 0, descriptor-publication counter at byte 64
+//   tmaps       TMA descriptors [capacity][A, B], 128 B each
+//   cta_prefix  [prefix_slots][cta_prefix_bytes(capacity)]  (capacity > 64 only)
+//   flags       uint32 [partial_slots]   epoch of the partial tile a CTA published
+//   partials    [partial_slots][128 x 256 fp32]  split-schedule partial tiles
+struct WorkspaceView {
+    uint32_t *status;
+    uint32_t *desc_count;
+    uint8_t *tmaps;
+    int32_t *cta_prefix;
+    uint32_t *flags;
+    float *partials;
+    int32_t capacity;
+    int32_t prefix_slots;
+    int32_t partial_slots;
+};
+
+constexpr size_t workspace_bytes(int capacity, int prefix_slots = 0, int partial_slots = 0) {
+    return 128 + (size_t)kDescBytes * 2 * (size_t)capacity +
+           (capacity > kMediumGroups ? cta_prefix_bytes(capacity) * (size_t)prefix_slots : 0) +
            (partial_slots > 0 ? round_up(sizeof(uint32_t) * (size_t)partial_slots, 128) +
                                     kPartialSlotBytes * (size_t)partial_slots
                               : 0);
 }
 
-inline WorkspaceView workspace_view(void *base, int capacity, int partial_slots = 0) {
+inline WorkspaceView workspace_view(void *base, int capacity, int prefix_slots = 0, int partial_slots = 0) {
     uint8_t *p = static_cast<uint8_t *>(base);
     WorkspaceView v;
     v.status = reinterpret_cast<uint32_t *>(p);
+    v.desc_count = reinterpret_cast<uint32_t *>(p + 64);
     p += 128;
-    v.prefix = reinterpret_cast<int32_t *>(p);
-    p += round_up(sizeof(int32_t) * (size_t)(capacity + 1), 128);
-    v.wprefix = reinterpret_cast<int32_t *>(p);
-    p += round_up(sizeof(int32_t) * (size_t)(capacity + 1), 128);
-    v.groups = reinterpret_cast<GroupInfo *>(p);
-    p += round_up(sizeof(GroupInfo) * (size_t)capacity, 128);
     v.tmaps = p;
-    p += 256 * (size_t)capacity;
+    p += (size_t)kDescBytes * 2 * (size_t)capacity;
+    v.cta_prefix = nullptr;
+    v.prefix_slots = 0;
+    if (capacity > kMediumGroups) {
+        v.cta_prefix = reinterpret_cast<int32_t *>(p);
+        v.prefix_slots = prefix_slots;
+        p += cta_prefix_bytes(capacity) * (size_t)prefix_slots;
+    }
     v.flags = nullptr;
     v.partials = nullptr;
     if (partial_slots > 0) {
@@ -103,25 +98,28 @@ inline WorkspaceView workspace_view(void *base, int capacity, int partial_slots 
 constexpr uint32_t kStatusProducerTimeout = 1u;
 constexpr uint32_t kStatusMmaTimeout = 2u;
 constexpr uint32_t kStatusEpilogueTimeout = 4u;
+constexpr uint32_t kStatusFlagTimeout = 8u;
+constexpr uint32_t kStatusDescTimeout = 16u;
 
 // Launch configuration chosen by the host for one call.
 struct GemmLaunch {
-    int block_n;          // 128 or 256
+    int block_n;            // 128 or 256
     int group_count;
-    int total_tiles;      // output tiles
-    int total_work;       // schedule units: sum over tiles of max(k-tiles, 1)
-    int grid;             // persistent CTAs
-    int split;            // 1: CTAs take equal ranges of schedule units (tiles may be split along K)
-    uint32_t epoch;       // tag of this call's partial-sum flags (split schedules)
-    uint64_t timeout_ns;  // bound of every wait
+    int desc_groups;        // groups with m, n, k > 0 (each gets a descriptor pair)
+    int total_tiles;        // output tiles
+    int total_work;         // schedule units: sum over tiles of max(k-tiles, 1)
+    int grid;               // persistent CTAs (all resident: cooperative launch)
+    int split;              // 1: CTAs take equal ranges of schedule units (tiles may be split along K)
+    uint32_t epoch;         // tag of this call's partial-tile flags (split schedules)
+    uint32_t desc_base;     // descriptor counter value before this call
+    uint64_t timeout_ns;    // bound of every wait
 };
 
-// Host launchers (gemm.cu). `tmpl_a` / `tmpl_b` are 128-byte encoded TMA
-// descriptors used as templates by the prologue.
+// Host launcher (gemm.cu). `tmpl_a` / `tmpl_b` are 128-byte encoded TMA
+// descriptors the kernel patches per group.
 cudaError_t launch_grouped(const GemmLaunch &cfg, const GroupArgs *groups, const WorkspaceView &ws,
                            const void *tmpl_a, const void *tmpl_b, cudaStream_t stream);
 cudaError_t prepare_gemm_kernels(int device);
-size_t gemm_smem_bytes(int block_n);
 
 // Host layer (api.cu), shared by the entry points.
 int fail(int status, const char *fmt, ...);
@@ -132,12 +130,17 @@ int check_groups(int group_count, int max_groups, const nvfp4_problem_size *prob
                  const void *const *B, const void *const *SFA, const void *const *SFB, void *const *C, int block_n,
                  GroupArgs *args, long long *total_tiles);
 int current_block_n();
+// Per-workspace host state of the calls that share it (in stream order).
+struct WorkspaceState {
+    uint32_t epoch = 0;       // last partial-tile epoch handed out
+    uint32_t desc_count = 0;  // expected descriptor counter before the next call
+};
 // Set up the current device on first use and launch a checked call whose
-// scratch is the workspace at ws_base (capacity groups).
-// With partial_slots > 0 and a non-null epoch counter the call may use a
-// split schedule (the counter tags its partial-sum flags).
+// scratch is the workspace at ws_base. With partial_slots > 0 the call may use
+// a split schedule.
 int launch_on_workspace(int group_count, const GroupArgs *args, long long total_tiles, int block_n, void *ws_base,
-                        int capacity, int partial_slots, uint32_t *epoch, cudaStream_t stream);
+                        int capacity, int prefix_slots, int partial_slots, WorkspaceState *state,
+                        cudaStream_t stream);
 
 // Packer launcher (pack_scales.cu).
 cudaError_t launch_pack_scales(const uint8_t *src, int rows, int k, uint8_t *dst, cudaStream_t stream);

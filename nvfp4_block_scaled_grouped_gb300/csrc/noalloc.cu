@@ -7,7 +7,7 @@
 // pre-planned arena and account for it, and latency-critical callers for whom
 // a cudaMalloc / cudaFree -- which may synchronise the whole device -- in the
 // middle of their work is not acceptable. nvfp4_grouped_gemm_noalloc runs the
-// same prologue and GEMM kernels with their scratch in the fixed array below
+// same GEMM kernel with its scratch in the fixed array below
 // instead, and never allocates.
 #include <cuda_runtime.h>
 
@@ -73,12 +73,13 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int group_count, const nvfp4_problem_s
     s = noalloc_workspace(device, &ws);
     if (s != NVFP4_OK)
         return s;
-    // The array keeps the previous call's contents. The prologue rewrites the
-    // prefix sum, group table and descriptors of this call; the status word
-    // is the one field that must start at zero.
+    // The array keeps the previous call's contents. Each call rewrites the
+    // descriptors it reads; the header (status word and the counter the
+    // descriptor patching counts up) must start at zero.
     e = cudaMemsetAsync(ws, 0, 128, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
-        return cuda_fail(e, "clearing the static workspace status word");
-    return launch_on_workspace(group_count, args, total, block_n, ws, NVFP4_NOALLOC_MAX_GROUPS, 0, nullptr,
+        return cuda_fail(e, "clearing the static workspace header");
+    WorkspaceState state;  // counter starts from the cleared header
+    return launch_on_workspace(group_count, args, total, block_n, ws, NVFP4_NOALLOC_MAX_GROUPS, 0, 0, &state,
                                reinterpret_cast<cudaStream_t>(stream));
 }
