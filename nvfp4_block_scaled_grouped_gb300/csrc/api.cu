@@ -180,7 +180,7 @@ int check_groups(int group_count, int max_groups, const nvfp4_problem_size *prob
         const nvfp4_problem_size &s = problem_sizes[g];
         if (s.m < 0 || s.n < 0 || s.k < 0 || s.l < 0)
             return fail(NVFP4_ERR_INVALID_ARG, "group %d: negative size (%d, %d, %d, %d)", g, s.m, s.n, s.k, s.l);
-        args[g] = GroupArgs{s.m, s.n, s.k, s.l, A[g], B[g], SFA[g], SFB[g], C[g]};
+        args[g] = GroupArgs{s.m, s.n, s.k, 3, A[g], B[g], SFA[g], SFB[g], C[g]};
         if (s.m == 0 || s.n == 0)
             continue;
         if (s.l != 1)
@@ -219,7 +219,7 @@ bool want_split(long long total_tiles, int sm_count) {
     return (double)waves >= 1.4 * (double)total_tiles / (double)sm_count;
 }
 
-int launch_on_workspace(int group_count, const GroupArgs *args, long long total_tiles, int block_n, void *ws_base,
+int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles, int block_n, void *ws_base,
                         int capacity, int prefix_slots, int partial_slots, WorkspaceState *state,
                         cudaStream_t stream) {
     int device = 0;
@@ -227,7 +227,6 @@ int launch_on_workspace(int group_count, const GroupArgs *args, long long total_
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaGetDevice");
     long long total_work = 0;
-    int desc_groups = 0;
     for (int g = 0; g < group_count; ++g) {
         const GroupArgs &a = args[g];
         if (a.m <= 0 || a.n <= 0)
@@ -235,15 +234,17 @@ int launch_on_workspace(int group_count, const GroupArgs *args, long long total_
         const long long tiles = (long long)((a.m + kBlockM - 1) / kBlockM) * ((a.n + block_n - 1) / block_n);
         const long long kt = (a.k + kBlockK - 1) / kBlockK;
         total_work += tiles * (kt > 1 ? kt : 1);
-        if (a.k > 0)
-            ++desc_groups;
     }
     if (total_work > 0x7fffffffLL)
         return fail(NVFP4_ERR_UNSUPPORTED, "more than 2^31 - 1 k-tiles in one call");
     DeviceState *st = nullptr;
     GemmLaunch cfg;
+    int desc_maps = 0;
+    // One lock over set-up, launch and bookkeeping: calls that share a
+    // workspace must reach the GPU in the order their descriptor counts and
+    // cache updates were taken.
+    std::lock_guard<std::mutex> lock(g_mutex);
     {
-        std::lock_guard<std::mutex> lock(g_mutex);
         int s = device_state(device, ws_base, &st);
         if (s != NVFP4_OK)
             return s;
@@ -259,12 +260,33 @@ int launch_on_workspace(int group_count, const GroupArgs *args, long long total_
         if (group_count > kMediumGroups && prefix_slots < cfg.grid)
             return fail(NVFP4_ERR_UNSUPPORTED, "workspace has %d CTA slots, the launch needs %d", prefix_slots,
                         cfg.grid);
+        // Descriptors to patch: those whose slot does not already hold this
+        // group's pointer and shape (the slots are written only by this
+        // workspace's calls, in stream order).
+        if (state->descs.size() < 2 * (size_t)capacity)
+            state->descs.assign(2 * (size_t)capacity, DescKey());
+        desc_maps = 0;
+        for (int g = 0; g < group_count; ++g) {
+            GroupArgs &a = args[g];
+            a.patch = 0;
+            if (a.m <= 0 || a.n <= 0 || a.k <= 0)
+                continue;
+            const DescKey ka{a.a, a.m, a.k, kBlockM}, kb{a.b, a.n, a.k, block_n};
+            if (!(state->descs[2 * g] == ka)) {
+                a.patch |= 1;
+                ++desc_maps;
+            }
+            if (!(state->descs[2 * g + 1] == kb)) {
+                a.patch |= 2;
+                ++desc_maps;
+            }
+        }
         cfg.desc_base = state->desc_count;
-        state->desc_count += (uint32_t)desc_groups;
+        state->desc_count += (uint32_t)desc_maps;
     }
     cfg.block_n = block_n;
     cfg.group_count = group_count;
-    cfg.desc_groups = desc_groups;
+    cfg.desc_maps = desc_maps;
     cfg.total_tiles = (int)total_tiles;
     cfg.total_work = (int)total_work;
     cfg.timeout_ns = watchdog_ns();
@@ -272,10 +294,16 @@ int launch_on_workspace(int group_count, const GroupArgs *args, long long total_
     const void *tmpl_b = block_n == 256 ? (const void *)&st->tmpl_b256 : (const void *)&st->tmpl_b128;
     e = launch_grouped(cfg, args, ws, &st->tmpl_a, tmpl_b, stream);
     if (e != cudaSuccess) {
-        // nothing ran: the device counter did not move
-        std::lock_guard<std::mutex> lock(g_mutex);
-        state->desc_count -= (uint32_t)desc_groups;
+        // nothing ran: the device counter did not move, no slot was written
+        state->desc_count -= (uint32_t)desc_maps;
         return cuda_fail(e, "grouped GEMM launch");
+    }
+    for (int g = 0; g < group_count; ++g) {
+        const GroupArgs &a = args[g];
+        if (a.patch & 1)
+            state->descs[2 * g] = DescKey{a.a, a.m, a.k, kBlockM};
+        if (a.patch & 2)
+            state->descs[2 * g + 1] = DescKey{a.b, a.n, a.k, block_n};
     }
     return NVFP4_OK;
 }

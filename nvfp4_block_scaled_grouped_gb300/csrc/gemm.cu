@@ -82,7 +82,7 @@ struct Cfg {
     static_assert(kSfColBase + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
     static constexpr int kThreads = 320;                           // 10 warps
     static constexpr int kBarrierBytes = 256;
-    static_assert((3 * kStages + 2 * kAccStages) * 8 <= 192, "barrier area");
+    static_assert((3 * kStages + 2 * kAccStages) * 8 <= 184, "barrier area");
     static constexpr int kEpiStageBytes = 32 * 64;                 // per epilogue warp: 32 rows x 32 fp16
     // Prefix sums live in shared memory for up to kMediumGroups groups, else
     // in the CTA's global scratch slot.
@@ -99,7 +99,7 @@ struct GemmParams {
     alignas(64) uint8_t tmpl_a[128];
     alignas(64) uint8_t tmpl_b[128];
     WorkspaceView ws;
-    int32_t group_count, block_n, total_tiles, total_work, split, desc_groups;
+    int32_t group_count, block_n, total_tiles, total_work, split, desc_maps;
     uint32_t epoch, desc_base;
     uint64_t timeout_ns;
     GroupArgs groups[CAP];
@@ -259,6 +259,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     auto sff_bar = [&](int s) { return bars + 8u * (2 * C::kStages + s); };
     auto accf_bar = [&](int a) { return bars + 8u * (3 * C::kStages + a); };
     auto acce_bar = [&](int a) { return bars + 8u * (3 * C::kStages + C::kAccStages + a); };
+    const uint32_t partial_bar = bars + 184;  // partial tile of a split tile landed in smem
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_area + 192);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 196);
     volatile int *s_epi_ok = reinterpret_cast<volatile int *>(bar_area + 208);
@@ -282,6 +283,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 ptx::mbar_init(accf_bar(a), 1);
                 ptx::mbar_init(acce_bar(a), 4);
             }
+            ptx::mbar_init(partial_bar, 1);
             *abort_flag = 0;
             ptx::fence_mbar_init();
         }
@@ -291,23 +293,20 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             const GroupArgs &a = p.groups[g];
             if (a.m <= 0 || a.n <= 0 || a.k <= 0)
                 continue;
-            uint8_t *ta = p.ws.tmaps + (size_t)g * 2 * kDescBytes;
-            uint8_t *tb = ta + kDescBytes;
-            const uint4 *src_a = reinterpret_cast<const uint4 *>(p.tmpl_a);
-            const uint4 *src_b = reinterpret_cast<const uint4 *>(p.tmpl_b);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                reinterpret_cast<uint4 *>(ta)[q] = src_a[q];
-                reinterpret_cast<uint4 *>(tb)[q] = src_b[q];
-            }
             const uint32_t row_bytes = (uint32_t)(a.k / 2);
-            ptx::tmap_set_address(ta, a.a);
-            ptx::tmap_set_dims(ta, row_bytes, (uint32_t)a.m);
-            ptx::tmap_set_stride1(ta, row_bytes);
-            ptx::tmap_set_address(tb, a.b);
-            ptx::tmap_set_dims(tb, row_bytes, (uint32_t)a.n);
-            ptx::tmap_set_stride1(tb, row_bytes);
-            ++patched;
+            for (int which = 0; which < 2; ++which) {
+                if (!(a.patch & (1 << which)))
+                    continue;
+                uint8_t *t = p.ws.tmaps + ((size_t)g * 2 + which) * kDescBytes;
+                const uint4 *src = reinterpret_cast<const uint4 *>(which ? p.tmpl_b : p.tmpl_a);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    reinterpret_cast<uint4 *>(t)[q] = src[q];
+                ptx::tmap_set_address(t, which ? a.b : a.a);
+                ptx::tmap_set_dims(t, row_bytes, (uint32_t)(which ? a.n : a.m));
+                ptx::tmap_set_stride1(t, row_bytes);
+                ++patched;
+            }
         }
         if (patched) {
             ptx::tmap_release();
@@ -369,7 +368,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
             int prev_g = -1;
-            bool descs_ready = p.desc_groups == 0;
+            bool descs_ready = p.desc_maps == 0;
             bool ok = true;
             Cursor<BN> cur = cursor0;
             Segment sg;
@@ -384,7 +383,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 const uint8_t *tmap_b = tmap_a + 128;
                 if (!descs_ready) {
                     // every group's descriptors are patched by some CTA at start-up
-                    if (!wait_counter(p.ws.desc_count, p.desc_base + (uint32_t)p.desc_groups, abort_flag,
+                    if (!wait_counter(p.ws.desc_count, p.desc_base + (uint32_t)p.desc_maps, abort_flag,
                                       p.timeout_ns, p.ws.status)) {
                         ok = false;
                         break;
@@ -557,6 +556,11 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             const bool zero = gi.k == 0;
             const bool cont = sg.kt0 > 0;                                       // a later piece of a split tile
             const bool finish_split = p.split && sg.kt0 == 0 && sg.kt1 < sg.ktg;  // first piece of a split tile
+            // CTAs cta+1 .. cta+pieces hold the later pieces of a split tile
+            int pieces = 0;
+            if (finish_split)
+                while (cta + pieces + 1 < ncta && split_begin(cta + pieces + 1, ncta, p.total_work) < sg.w_tile_end)
+                    ++pieces;
             // One thread waits (for the accumulator and, when finishing a split
             // tile, for the later pieces' flags); the four warps leave or stay
             // together: the TMEM loads below are warp-collective.
@@ -566,7 +570,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                              ? 1
                              : 0;
                 if (ok && finish_split) {
-                    for (int c2 = cta + 1; c2 < ncta && split_begin(c2, ncta, p.total_work) < sg.w_tile_end; ++c2) {
+                    for (int c2 = cta + 1; c2 <= cta + pieces; ++c2) {
                         const uint64_t t0 = ptx::globaltimer();
                         while (ptx::ld_acquire_gpu(p.ws.flags + c2) != p.epoch) {
                             if (ptx::globaltimer() - t0 > p.timeout_ns) {
@@ -579,12 +583,31 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                         if (!ok)
                             break;
                     }
+                    if (ok) {
+                        // A split tile is always its finishing CTA's last
+                        // segment: every MMA has completed, no copy is pending,
+                        // so the stage ring is free. The next piece's partial
+                        // tile moves there with bulk copies (16 KiB per chunk).
+                        const int nch = (gi.n - sg.tn * BN) / 32 < BN / 32 ? (gi.n - sg.tn * BN) / 32 : BN / 32;
+                        const char *src = reinterpret_cast<const char *>(p.ws.partials) +
+                                          (size_t)(cta + 1) * kPartialSlotBytes;
+                        ptx::mbar_arrive_expect_tx(partial_bar, (uint32_t)nch * 8 * kBlockM * 16);
+                        for (int cc = 0; cc < nch; ++cc)
+                            ptx::bulk_load(smem_base + cc * 8 * kBlockM * 16, src + (size_t)cc * 8 * kBlockM * 16,
+                                           8 * kBlockM * 16, partial_bar, ptx::l2_policy_evict_first());
+                        ok = wait_bounded(partial_bar, 0, abort_flag, p.timeout_ns, p.ws.status,
+                                          kStatusFlagTimeout)
+                                 ? 1
+                                 : 0;
+                    }
                 }
                 *s_epi_ok = ok;
             }
             ptx::named_barrier(1, 128);
             if (!*s_epi_ok)
                 break;
+            if (finish_split)
+                (void)ptx::mbar_try_wait(partial_bar, 0);  // every thread acquires the landed partial tile
             ptx::tc_fence_after();
             const int row = sg.tm * kBlockM + r_local;
             const uint32_t t_row = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * C::kAccCols);
@@ -595,84 +618,18 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             // finishing a split tile, the first later piece's next chunk is
             // loaded while the current one is converted (L2 latency hidden).
             const int nchunks = (n - sg.tn * BN) / 32 < BN / 32 ? (n - sg.tn * BN) / 32 : BN / 32;
-            const bool prefetch = finish_split && row < m;
-            float4 pf[8];
-            if (prefetch) {
-                const float4 *src = reinterpret_cast<const float4 *>(p.ws.partials) +
-                                    (size_t)(cta + 1) * (kPartialSlotBytes / 16) + r_local;
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    pf[q] = __ldcg(src + q * kBlockM);
-            }
-#pragma unroll 1
-            for (int cc = 0; cc < nchunks; ++cc) {
+            // fp16 row segment (64 B, 16 words) of chunk cc -> this warp's
+            // staging buffer, 16-byte pieces XOR-swizzled by (row / 2) % 4 so
+            // that neither the row-wise writes nor the transposed reads conflict
+            // on banks; then 4 lanes per row, each store writing 8 rows x 64 B.
+            auto store_chunk = [&](const int cc, const uint32_t (&h)[16]) {
                 const int col = sg.tn * BN + cc * 32;
-                uint32_t v[32];
-                ptx::tmem_ld_32x32b_x32(t_row + cc * 32, v);
-                ptx::tmem_ld_wait();
-                float4 *part = reinterpret_cast<float4 *>(p.ws.partials) + ((size_t)cc * 8) * kBlockM + r_local;
-                if (cont) {
-                    if (row < m) {
-                        float4 *dst = part + (size_t)cta * (kPartialSlotBytes / 16);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[q * kBlockM] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                                           __uint_as_float(v[4 * q + 2]),
-                                                           __uint_as_float(v[4 * q + 3]));
-                    }
-                    continue;
-                }
-                float f[32];
-#pragma unroll
-                for (int q = 0; q < 32; ++q)
-                    f[q] = zero ? 0.0f : __uint_as_float(v[q]);
-                if (prefetch) {
-                    float4 cur[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        cur[q] = pf[q];
-                    if (cc + 1 < nchunks) {
-                        const float4 *src = part + 8 * kBlockM + (size_t)(cta + 1) * (kPartialSlotBytes / 16);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            pf[q] = __ldcg(src + q * kBlockM);
-                    }
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        f[4 * q] += cur[q].x;
-                        f[4 * q + 1] += cur[q].y;
-                        f[4 * q + 2] += cur[q].z;
-                        f[4 * q + 3] += cur[q].w;
-                    }
-                    // further pieces of the same tile (rare: a tile spanning 3+ CTAs)
-                    for (int c2 = cta + 2; c2 < ncta && split_begin(c2, ncta, p.total_work) < sg.w_tile_end; ++c2) {
-                        const float4 *src = part + (size_t)c2 * (kPartialSlotBytes / 16);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const float4 p4 = __ldcg(src + q * kBlockM);
-                            f[4 * q] += p4.x;
-                            f[4 * q + 1] += p4.y;
-                            f[4 * q + 2] += p4.z;
-                            f[4 * q + 3] += p4.w;
-                        }
-                    }
-                }
-                // fp16 row segment (64 B) -> this warp's staging buffer, 16-byte
-                // pieces XOR-swizzled by (row / 2) % 4 so that neither the
-                // row-wise writes nor the transposed reads conflict on banks.
-                uint32_t h[16];
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    __half2 p2 = __floats2half2_rn(f[2 * q], f[2 * q + 1]);
-                    h[q] = *reinterpret_cast<uint32_t *>(&p2);
-                }
                 const int sw = (lane >> 1) & 3;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     *reinterpret_cast<uint4 *>(buf + lane * 64 + 16 * (j ^ sw)) =
                         make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
                 __syncwarp();
-                // 4 lanes per row: each store instruction writes 8 rows x 64 B.
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int r = 8 * q + (lane >> 2);
@@ -683,6 +640,91 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                         *reinterpret_cast<uint4 *>(c_base + (size_t)grow * (size_t)n + col + 8 * piece) = val;
                 }
                 __syncwarp();
+            };
+            auto pack = [&](float x0, float x1) {
+                __half2 h2 = __floats2half2_rn(x0, x1);
+                return *reinterpret_cast<uint32_t *>(&h2);
+            };
+            if (cont) {
+                // later piece of a split tile: fp32 partial tile to this CTA's
+                // slot; TMEM loads run half a chunk ahead of the stores
+                float4 *dst = reinterpret_cast<float4 *>(p.ws.partials) + (size_t)cta * (kPartialSlotBytes / 16) + r_local;
+                auto put = [&](const uint32_t (&v)[16], float4 *d) {
+                    if (row < m) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            d[q * kBlockM] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                         __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                    }
+                };
+                uint32_t va[16], vb[16];
+                ptx::tmem_ld_32x32b_x16(t_row, va);
+#pragma unroll 1
+                for (int cc = 0; cc < nchunks; ++cc) {
+                    ptx::tmem_ld_wait();
+                    ptx::tmem_ld_32x32b_x16(t_row + cc * 32 + 16, vb);
+                    put(va, dst + (size_t)cc * 8 * kBlockM);
+                    ptx::tmem_ld_wait();
+                    if (cc + 1 < nchunks)
+                        ptx::tmem_ld_32x32b_x16(t_row + (cc + 1) * 32, va);
+                    put(vb, dst + ((size_t)cc * 8 + 4) * kBlockM);
+                }
+            } else if (finish_split) {
+                // first piece of a split tile: add the later pieces' partial
+                // tiles (the next piece's from shared memory, any further
+                // ones -- a tile spanning 3+ CTAs -- from L2)
+                const float4 *sp = reinterpret_cast<const float4 *>(smem) + r_local;
+#pragma unroll 1
+                for (int cc = 0; cc < nchunks; ++cc) {
+                    uint32_t v[32];
+                    ptx::tmem_ld_32x32b_x32(t_row + cc * 32, v);
+                    ptx::tmem_ld_wait();
+                    const float4 *part = reinterpret_cast<const float4 *>(p.ws.partials) + ((size_t)cc * 8) * kBlockM +
+                                         r_local;
+                    uint32_t h[16];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        float x0 = __uint_as_float(v[4 * q]), x1 = __uint_as_float(v[4 * q + 1]);
+                        float x2 = __uint_as_float(v[4 * q + 2]), x3 = __uint_as_float(v[4 * q + 3]);
+                        if (row < m) {
+                            const float4 cur = sp[(cc * 8 + q) * kBlockM];
+                            x0 += cur.x;
+                            x1 += cur.y;
+                            x2 += cur.z;
+                            x3 += cur.w;
+                            for (int c2 = cta + 2; c2 <= cta + pieces; ++c2) {
+                                const float4 p4 = __ldcg(part + (size_t)c2 * (kPartialSlotBytes / 16) + q * kBlockM);
+                                x0 += p4.x;
+                                x1 += p4.y;
+                                x2 += p4.z;
+                                x3 += p4.w;
+                            }
+                        }
+                        h[2 * q] = pack(x0, x1);
+                        h[2 * q + 1] = pack(x2, x3);
+                    }
+                    store_chunk(cc, h);
+                }
+            } else {
+                // whole tile: TMEM loads run half a chunk (16 columns) ahead of
+                // the conversion and stores
+                uint32_t va[16], vb[16], h[16];
+                ptx::tmem_ld_32x32b_x16(t_row, va);
+#pragma unroll 1
+                for (int cc = 0; cc < nchunks; ++cc) {
+                    ptx::tmem_ld_wait();
+                    ptx::tmem_ld_32x32b_x16(t_row + cc * 32 + 16, vb);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        h[q] = zero ? 0u : pack(__uint_as_float(va[2 * q]), __uint_as_float(va[2 * q + 1]));
+                    ptx::tmem_ld_wait();
+                    if (cc + 1 < nchunks)
+                        ptx::tmem_ld_32x32b_x16(t_row + (cc + 1) * 32, va);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        h[8 + q] = zero ? 0u : pack(__uint_as_float(vb[2 * q]), __uint_as_float(vb[2 * q + 1]));
+                    store_chunk(cc, h);
+                }
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -725,7 +767,7 @@ cudaError_t launch_cap(const GemmLaunch &cfg, const GroupArgs *groups, const Wor
     prm.total_tiles = cfg.total_tiles;
     prm.total_work = cfg.total_work;
     prm.split = cfg.split;
-    prm.desc_groups = cfg.desc_groups;
+    prm.desc_maps = cfg.desc_maps;
     prm.epoch = cfg.epoch;
     prm.desc_base = cfg.desc_base;
     prm.timeout_ns = cfg.timeout_ns;

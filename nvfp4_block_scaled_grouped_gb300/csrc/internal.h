@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -20,8 +21,10 @@ constexpr int kMmaK = 64;
 constexpr int kSfAtomBytes = 512;  // 128 rows x 4 scale blocks
 
 // A group's arguments, passed to the GEMM kernel as a kernel parameter.
+// `patch` tells the kernel which of the group's descriptors (bit 0: A, bit 1:
+// B) must be rewritten; the others already hold this group's pointer and shape.
 struct GroupArgs {
-    int32_t m, n, k, l;
+    int32_t m, n, k, patch;
     const void *a, *b, *sfa, *sfb;
     void *c;
 };
@@ -105,7 +108,7 @@ constexpr uint32_t kStatusDescTimeout = 16u;
 struct GemmLaunch {
     int block_n;            // 128 or 256
     int group_count;
-    int desc_groups;        // groups with m, n, k > 0 (each gets a descriptor pair)
+    int desc_maps;          // descriptors the kernel patches (bits set in GroupArgs::patch)
     int total_tiles;        // output tiles
     int total_work;         // schedule units: sum over tiles of max(k-tiles, 1)
     int grid;               // persistent CTAs (all resident: cooperative launch)
@@ -130,15 +133,22 @@ int check_groups(int group_count, int max_groups, const nvfp4_problem_size *prob
                  const void *const *B, const void *const *SFA, const void *const *SFB, void *const *C, int block_n,
                  GroupArgs *args, long long *total_tiles);
 int current_block_n();
+// What one descriptor slot holds: base address, rows, k and the box height.
+struct DescKey {
+    const void *ptr = nullptr;
+    int32_t rows = 0, k = 0, box = 0;
+    bool operator==(const DescKey &o) const { return ptr == o.ptr && rows == o.rows && k == o.k && box == o.box; }
+};
 // Per-workspace host state of the calls that share it (in stream order).
 struct WorkspaceState {
-    uint32_t epoch = 0;       // last partial-tile epoch handed out
-    uint32_t desc_count = 0;  // expected descriptor counter before the next call
+    uint32_t epoch = 0;            // last partial-tile epoch handed out
+    uint32_t desc_count = 0;       // expected descriptor counter before the next call
+    std::vector<DescKey> descs;    // [group][A, B]: what each descriptor slot holds (empty: unknown)
 };
 // Set up the current device on first use and launch a checked call whose
 // scratch is the workspace at ws_base. With partial_slots > 0 the call may use
 // a split schedule.
-int launch_on_workspace(int group_count, const GroupArgs *args, long long total_tiles, int block_n, void *ws_base,
+int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles, int block_n, void *ws_base,
                         int capacity, int prefix_slots, int partial_slots, WorkspaceState *state,
                         cudaStream_t stream);
 

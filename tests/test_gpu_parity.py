@@ -239,3 +239,41 @@ def test_two_streams_concurrently(nv, oracle_mod):
         for g, (c, r) in enumerate(zip(dp.c_host(), _oracle_full(oracle_mod, prob))):
             assert_parity(c, r, f"stream problem group {g}")
     assert nv.device_status(s1) == 0 and nv.device_status(s2) == 0
+
+
+def test_descriptor_slots_follow_pointer_and_shape_changes(nv, oracle_mod):
+    """A workspace's descriptor slots are reused across calls when a group's
+    pointer and shape are unchanged; any change (groups reordered, a smaller m
+    over the same buffer, another tile width) must be patched again."""
+    from nvfp4_block_scaled_grouped_gb300.device import DeviceProblem
+    sizes = [(130, 256, 512, 1), (64, 128, 256, 1), (200, 384, 768, 1)]
+    prob = _make(sizes, seed=31)
+    dp = DeviceProblem.upload(prob)
+    ref = _oracle_full(oracle_mod, prob)
+
+    def check(order, msg, block_n=256):
+        nv.set_tile_n(block_n)
+        out = [torch.full_like(dp.C[g], float("nan")) for g in order]
+        nv.grouped_gemm([sizes[g] for g in order], [dp.A[g].data_ptr() for g in order],
+                        [dp.B[g].data_ptr() for g in order], [dp.SFA[g].data_ptr() for g in order],
+                        [dp.SFB[g].data_ptr() for g in order], [o.data_ptr() for o in out])
+        torch.cuda.synchronize()
+        assert nv.device_status() == 0
+        for i, g in enumerate(order):
+            assert_parity(out[i].cpu().numpy(), ref[g], f"{msg}: slot {i} = group {g}")
+
+    check([0, 1, 2], "first call")
+    check([0, 1, 2], "same pointers and shapes again")
+    check([2, 0, 1], "groups moved to other slots")
+    check([2, 0, 1], "moved groups, BN=128", block_n=128)
+    check([2, 0, 1], "moved groups, back to BN=256")
+    # the same A buffer read as fewer rows: only m changes
+    m_small = 70
+    sub = _make([(m_small, 256, 512, 1)], seed=31)  # same seed/stream: rows are a prefix of group 0
+    np.testing.assert_array_equal(sub.A[0], prob.A[0][:m_small])
+    out = torch.full((m_small, 256), float("nan"), dtype=torch.float16, device="cuda")
+    sfa_small = nv.pack_scales_tensor(torch.from_numpy(prob.SFA[0][:m_small]).cuda(), 512)
+    nv.grouped_gemm([(m_small, 256, 512, 1)], [dp.A[0].data_ptr()], [dp.B[0].data_ptr()],
+                    [sfa_small.data_ptr()], [dp.SFB[0].data_ptr()], [out.data_ptr()])
+    torch.cuda.synchronize()
+    assert_parity(out.cpu().numpy(), ref[0][:m_small], "m shrunk over the same A buffer")
