@@ -316,38 +316,26 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::kTmemCols);
         ptx::tmem_relinquish();
     } else if (warp == 6) {
-        // Exclusive prefix sums of output tiles and schedule units per group:
-        // lane l takes a contiguous run of groups, then one warp scan.
-        const int per = (group_count + 31) / 32;
-        const int g0 = lane * per;
-        const int g1 = (g0 + per) < group_count ? (g0 + per) : group_count;
-        int st = 0, sw = 0;
-        for (int g = g0; g < g1; ++g) {
-            const GInfo gi = group_info<BN>(p.groups[g]);
-            st += gi.tiles;
-            sw += gi.tiles * gi.work_tiles;
-        }
-        int it = st, iw = sw;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int yt = __shfl_up_sync(0xffffffffu, it, off);
-            const int yw = __shfl_up_sync(0xffffffffu, iw, off);
-            if (lane >= off) {
-                it += yt;
-                iw += yw;
+        // Exclusive prefix sums of output tiles and schedule units per group.
+        // The group table lives in the constant bank, where a warp reading
+        // different addresses is serialised, so every lane walks all groups
+        // with the same index (broadcast reads) and lane g % 32 stores entry g.
+        int bt = 0, bw = 0;
+#pragma unroll 4
+        for (int g = 0; g < group_count; ++g) {
+            const GroupArgs &a = p.groups[g];
+            const int tiles = (a.m > 0 && a.n > 0) ? ceil_div_i(a.m, kBlockM) * ceil_div_i(a.n, BN) : 0;
+            const int kt = ceil_div_i(a.k, kBlockK);
+            if (lane == (g & 31)) {
+                prefix[g] = bt;
+                wprefix[g] = bw;
             }
+            bt += tiles;
+            bw += tiles * (kt > 1 ? kt : 1);
         }
-        int bt = it - st, bw = iw - sw;
-        for (int g = g0; g < g1; ++g) {
-            const GInfo gi = group_info<BN>(p.groups[g]);
-            prefix[g] = bt;
-            wprefix[g] = bw;
-            bt += gi.tiles;
-            bw += gi.tiles * gi.work_tiles;
-        }
-        if (lane == 31) {
-            prefix[group_count] = it;
-            wprefix[group_count] = iw;
+        if (lane == 0) {
+            prefix[group_count] = bt;
+            wprefix[group_count] = bw;
         }
     }
     ptx::tc_fence_before();
