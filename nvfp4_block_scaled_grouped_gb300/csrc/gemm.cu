@@ -60,6 +60,8 @@
 namespace nvfp4 {
 namespace {
 
+constexpr int kPartialChunkBytes = 8 * kBlockM * 16;  // one 32-column chunk of an fp32 partial tile
+
 template <int BN, int CAP>
 struct Cfg {
     static_assert(BN == 128 || BN == 256, "BLOCK_N");
@@ -81,9 +83,15 @@ struct Cfg {
     static constexpr int kTmemCols = 512;
     static_assert(kSfColBase + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
     static constexpr int kThreads = 320;                           // 10 warps
-    static constexpr int kBarrierBytes = 256;
+    static constexpr int kBarrierBytes = 384;
     static_assert((3 * kStages + 2 * kAccStages) * 8 <= 184, "barrier area");
     static constexpr int kEpiStageBytes = 32 * 64;                 // per epilogue warp: 32 rows x 32 fp16
+    // A finishing CTA receives the next piece's partial tile in ring stages,
+    // kPartialChunksPerStage 16 KiB chunks (32 columns x 128 rows fp32) per
+    // stage from offset 0; the last kEpiStageBytes of stages 0..3 are the
+    // staging buffers of the four helper warps that join the last epilogue.
+    static constexpr int kPartialChunksPerStage = (kStageBytes - kEpiStageBytes) / kPartialChunkBytes;
+    static_assert(kStages >= 4 && kPartialChunksPerStage * kStages >= BN / 32, "partial tile in the ring");
     // Prefix sums live in shared memory for up to kMediumGroups groups, else
     // in the CTA's global scratch slot.
     static constexpr bool kSmemPrefix = CAP <= kMediumGroups;
@@ -242,6 +250,166 @@ struct Cursor {
     }
 };
 
+// What the epilogue does with a segment's accumulator.
+enum : int {
+    kEpiWhole = 0,   // whole tile: fp16 to C
+    kEpiCont = 1,    // later piece of a split tile: fp32 partial tile to this CTA's workspace slot
+    kEpiFinish = 2,  // first piece of a split tile: add the later pieces' partial tiles, fp16 to C
+};
+
+// Hand-over of a CTA's last segment, which is finished after every role has
+// left its loop by the epilogue warps together with warps 4..7.
+struct TailState {
+    Segment seg;
+    int32_t valid, acc, acc_phase;
+    int32_t part_state;   // 1: the producer issued the next piece's partial-tile copies on partial_bar
+    int32_t part_ok;      // ... and every one of them
+    int32_t part_stage0;  // ring stage of the first partial chunk
+    int32_t pieces;       // later pieces of the finishing tile (CTAs blockIdx + 1 ..)
+};
+
+// Column chunks (32 columns) of a tile that hold columns < n.
+template <int BN>
+__device__ __forceinline__ int tile_chunks(const GInfo &gi, const Segment &sg) {
+    const int c = (gi.n - sg.tn * BN) / 32;
+    return c < BN / 32 ? c : BN / 32;
+}
+
+// One warp's share of a segment's epilogue: accumulator lanes 32 * quarter ..
+// +31 (tile rows), column chunks [c0, c1). TMEM loads run half a chunk (16
+// columns) ahead of the arithmetic and stores. `buf` is the warp's 2 KiB
+// staging buffer; `smem` the CTA's ring (holding the next piece's partial tile
+// from stage part_stage0 when finishing a split tile).
+template <int BN, int CAP>
+__device__ __forceinline__ void epilogue_warp(const GemmParams<CAP> &p, const Segment &sg, const GInfo &gi,
+                                              const int kind, const int quarter, const int lane,
+                                              const uint32_t t_acc, const int c0, const int c1, uint8_t *buf,
+                                              const uint8_t *smem, const int part_stage0, const int pieces) {
+    using C = Cfg<BN, CAP>;
+    if (c0 >= c1)
+        return;
+    const int m = gi.m, n = gi.n;
+    const int cta = blockIdx.x;
+    const int r_local = quarter * 32 + lane;
+    const int row = sg.tm * kBlockM + r_local;
+    const uint32_t t_row = t_acc + ((uint32_t)(quarter * 32) << 16);
+    __half *c_base = static_cast<__half *>(gi.c);
+    // fp16 row segment (64 B, 16 words) of chunk cc -> the staging buffer,
+    // 16-byte pieces XOR-swizzled by (row / 2) % 4 so that neither the
+    // row-wise writes nor the transposed reads conflict on banks; then 4 lanes
+    // per row, each store writing 8 rows x 64 B.
+    auto store_chunk = [&](const int cc, const uint32_t (&h)[16]) {
+        const int col = sg.tn * BN + cc * 32;
+        const int sw = (lane >> 1) & 3;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4 *>(buf + lane * 64 + 16 * (j ^ sw)) =
+                make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int r = 8 * q + (lane >> 2);
+            const int piece = lane & 3;
+            const uint4 val = *reinterpret_cast<const uint4 *>(buf + r * 64 + 16 * (piece ^ ((r >> 1) & 3)));
+            const int grow = sg.tm * kBlockM + quarter * 32 + r;
+            if (grow < m)
+                *reinterpret_cast<uint4 *>(c_base + (size_t)grow * (size_t)n + col + 8 * piece) = val;
+        }
+        __syncwarp();
+    };
+    auto pack = [](float x0, float x1) {
+        __half2 h2 = __floats2half2_rn(x0, x1);
+        return *reinterpret_cast<uint32_t *>(&h2);
+    };
+    // Partial tiles: [chunk][quad q][row] of float4, so a warp's stores and
+    // loads of one (chunk, q) cover 512 contiguous bytes.
+    uint32_t va[16], vb[16];
+    ptx::tmem_ld_32x32b_x16(t_row + c0 * 32, va);
+    if (kind == kEpiCont) {
+        float4 *dst = reinterpret_cast<float4 *>(p.ws.partials) + (size_t)cta * (kPartialSlotBytes / 16) + r_local;
+        auto put = [&](const uint32_t (&v)[16], float4 *d) {
+            if (row < m) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    d[q * kBlockM] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+            }
+        };
+#pragma unroll 1
+        for (int cc = c0; cc < c1; ++cc) {
+            ptx::tmem_ld_wait();
+            ptx::tmem_ld_32x32b_x16(t_row + cc * 32 + 16, vb);
+            put(va, dst + (size_t)cc * 8 * kBlockM);
+            ptx::tmem_ld_wait();
+            if (cc + 1 < c1)
+                ptx::tmem_ld_32x32b_x16(t_row + (cc + 1) * 32, va);
+            put(vb, dst + ((size_t)cc * 8 + 4) * kBlockM);
+        }
+    } else if (kind == kEpiFinish) {
+        // the next piece's partial from the ring, any further ones (a tile
+        // spanning 3+ CTAs) from L2
+        const float4 *gpart = reinterpret_cast<const float4 *>(p.ws.partials) + r_local;
+        auto add_half = [&](const uint32_t (&v)[16], const int cc, const int q0, uint32_t *h) {
+            const float4 *sp =
+                reinterpret_cast<const float4 *>(
+                    smem + ((part_stage0 + cc / C::kPartialChunksPerStage) % C::kStages) * C::kStageBytes +
+                    (cc % C::kPartialChunksPerStage) * kPartialChunkBytes) +
+                r_local;
+            // (rows >= m hold no partial values; their sums are never stored)
+            float4 a[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                a[q] = sp[(q0 + q) * kBlockM];
+            for (int c2 = cta + 2; c2 <= cta + pieces; ++c2) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 b =
+                        __ldcg(gpart + (size_t)c2 * (kPartialSlotBytes / 16) + ((size_t)cc * 8 + q0 + q) * kBlockM);
+                    a[q].x += b.x;
+                    a[q].y += b.y;
+                    a[q].z += b.z;
+                    a[q].w += b.w;
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                h[2 * q] = pack(__uint_as_float(v[4 * q]) + a[q].x, __uint_as_float(v[4 * q + 1]) + a[q].y);
+                h[2 * q + 1] = pack(__uint_as_float(v[4 * q + 2]) + a[q].z, __uint_as_float(v[4 * q + 3]) + a[q].w);
+            }
+        };
+        uint32_t h[16];
+#pragma unroll 1
+        for (int cc = c0; cc < c1; ++cc) {
+            ptx::tmem_ld_wait();
+            ptx::tmem_ld_32x32b_x16(t_row + cc * 32 + 16, vb);
+            add_half(va, cc, 0, h);
+            ptx::tmem_ld_wait();
+            if (cc + 1 < c1)
+                ptx::tmem_ld_32x32b_x16(t_row + (cc + 1) * 32, va);
+            add_half(vb, cc, 4, h + 8);
+            store_chunk(cc, h);
+        }
+    } else {
+        const bool zero = gi.k == 0;
+        uint32_t h[16];
+#pragma unroll 1
+        for (int cc = c0; cc < c1; ++cc) {
+            ptx::tmem_ld_wait();
+            ptx::tmem_ld_32x32b_x16(t_row + cc * 32 + 16, vb);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                h[q] = zero ? 0u : pack(__uint_as_float(va[2 * q]), __uint_as_float(va[2 * q + 1]));
+            ptx::tmem_ld_wait();
+            if (cc + 1 < c1)
+                ptx::tmem_ld_32x32b_x16(t_row + (cc + 1) * 32, va);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                h[8 + q] = zero ? 0u : pack(__uint_as_float(vb[2 * q]), __uint_as_float(vb[2 * q + 1]));
+            store_chunk(cc, h);
+        }
+    }
+}
+
 template <int BN, int CAP>
 __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams<CAP> p) {
     using C = Cfg<BN, CAP>;
@@ -262,7 +430,9 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     const uint32_t partial_bar = bars + 184;  // partial tile of a split tile landed in smem
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_area + 192);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 196);
-    volatile int *s_epi_ok = reinterpret_cast<volatile int *>(bar_area + 208);
+    volatile int *s_epi_ok = reinterpret_cast<volatile int *>(bar_area + 208);  // [3]: by segment parity, tail
+    TailState *s_tail = reinterpret_cast<TailState *>(bar_area + 256);
+    static_assert(256 + sizeof(TailState) <= C::kBarrierBytes, "barrier area");
     uint8_t *epi_stage = bar_area + C::kBarrierBytes;                // [4 warps][32 rows][64 B]
     int32_t *prefix;
     if constexpr (C::kSmemPrefix)
@@ -285,6 +455,11 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             }
             ptx::mbar_init(partial_bar, 1);
             *abort_flag = 0;
+            s_tail->valid = 0;
+            s_tail->part_state = 0;
+            s_tail->part_ok = 0;
+            s_tail->part_stage0 = 0;
+            s_tail->pieces = 0;
             ptx::fence_mbar_init();
         }
         // Patch the descriptors of this CTA's share of the groups.
@@ -312,6 +487,12 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             ptx::tmap_release();
             ptx::red_release_add_gpu(p.ws.desc_count, patched);
         }
+        // The producer needs the barriers and the prefix sums, not TMEM: it
+        // starts once warp 6 has the prefix sums, while the TMEM allocation
+        // may still be in progress.
+        __syncwarp();
+        ptx::named_barrier(2, 64);
+        ptx::named_barrier_arrive(3, C::kThreads);
     } else if (warp == 5) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::kTmemCols);
         ptx::tmem_relinquish();
@@ -337,11 +518,16 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             prefix[group_count] = bt;
             wprefix[group_count] = bw;
         }
+        __syncwarp();
+        ptx::named_barrier_arrive(2, 64);
     }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
+    uint32_t tmem_base = 0;  // warp 4 reads it after the role loops
+    if (warp != 4) {
+        ptx::tc_fence_before();
+        ptx::named_barrier(3, C::kThreads);
+        ptx::tc_fence_after();
+        tmem_base = *tmem_slot;
+    }
     const Cursor<BN> cursor0{prefix, wprefix, p.groups, group_count, p.split,
                              split_begin(blockIdx.x, gridDim.x, p.total_work),
                              split_begin(blockIdx.x + 1, gridDim.x, p.total_work),
@@ -360,7 +546,9 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             bool ok = true;
             Cursor<BN> cur = cursor0;
             Segment sg;
+            bool any = false;
             while (ok && cur.next(sg)) {
+                any = true;
                 const GInfo gi = group_info<BN>(p.groups[sg.g]);
                 const int k_tiles = gi.k_tiles;
                 const int kend = sg.kt1 < k_tiles ? sg.kt1 : k_tiles;
@@ -411,6 +599,59 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                         stage = 0;
                         phase ^= 1u;
                     }
+                }
+            }
+            if (ok && any && p.split && sg.kt0 == 0 && sg.kt1 < sg.ktg && !*abort_flag) {
+                // The last segment is the first piece of a split tile. Once the
+                // later pieces are published (they are their CTAs' first
+                // segments, so usually long before), the next piece's partial
+                // tile is copied into the ring, each stage as soon as the MMAs
+                // reading it have completed, oldest stage first.
+                const int cta = blockIdx.x, ncta = gridDim.x;
+                int pieces = 0;
+                while (cta + pieces + 1 < ncta && split_begin(cta + pieces + 1, ncta, p.total_work) < sg.w_tile_end)
+                    ++pieces;
+                bool flags_ok = true;
+                for (int c2 = cta + 1; c2 <= cta + pieces && flags_ok; ++c2) {
+                    const uint64_t t0 = ptx::globaltimer();
+                    while (ptx::ld_acquire_gpu(p.ws.flags + c2) != p.epoch) {
+                        if (*abort_flag) {
+                            flags_ok = false;
+                            break;
+                        }
+                        if (ptx::globaltimer() - t0 > p.timeout_ns) {
+                            *abort_flag = 1;
+                            atomicOr(p.ws.status, kStatusFlagTimeout);
+                            flags_ok = false;
+                            break;
+                        }
+                    }
+                }
+                s_tail->pieces = pieces;
+                if (flags_ok) {
+                    ptx::fence_proxy_async_global();
+                    const int nch = tile_chunks<BN>(group_info<BN>(p.groups[sg.g]), sg);
+                    const char *src =
+                        reinterpret_cast<const char *>(p.ws.partials) + (size_t)(cta + 1) * kPartialSlotBytes;
+                    bool good = true;
+                    for (int cc = 0; cc < nch; ++cc) {
+                        const int s = (stage + cc / C::kPartialChunksPerStage) % C::kStages;
+                        if (cc % C::kPartialChunksPerStage == 0 && ((armed >> s) & 1u) &&
+                            !wait_bounded(empty_bar(s), (armed_parity >> s) & 1u, abort_flag, p.timeout_ns,
+                                          p.ws.status, kStatusProducerTimeout)) {
+                            good = false;
+                            break;
+                        }
+                        ptx::mbar_expect_tx(partial_bar, kPartialChunkBytes);
+                        ptx::bulk_load(smem_base + s * C::kStageBytes + (cc % C::kPartialChunksPerStage) *
+                                                                            kPartialChunkBytes,
+                                       src + (size_t)cc * kPartialChunkBytes, kPartialChunkBytes, partial_bar,
+                                       ptx::l2_policy_evict_first());
+                    }
+                    ptx::mbar_arrive(partial_bar);
+                    s_tail->part_stage0 = stage;
+                    s_tail->part_ok = good ? 1 : 0;
+                    s_tail->part_state = 1;
                 }
             }
             if (!ok || *abort_flag) {
@@ -532,193 +773,42 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         }
     } else {
         // ===================== epilogue (warps 0..3) =====================
-        const int cta = blockIdx.x, ncta = gridDim.x;
-        const int r_local = warp * 32 + lane;
-        int acc = 0;
+        // Every segment but the CTA's last; the last is finished below, once
+        // every role has left its loop, with warps 4..7 helping.
+        const int cta = blockIdx.x;
+        int acc = 0, it = 0;
         uint32_t acc_phase = 0;
+        bool ok = true;
         Cursor<BN> cur = cursor0;
         Segment sg;
-        while (cur.next(sg)) {
-            const GInfo gi = group_info<BN>(p.groups[sg.g]);
-            const int m = gi.m, n = gi.n;
-            const bool zero = gi.k == 0;
-            const bool cont = sg.kt0 > 0;                                       // a later piece of a split tile
-            const bool finish_split = p.split && sg.kt0 == 0 && sg.kt1 < sg.ktg;  // first piece of a split tile
-            // CTAs cta+1 .. cta+pieces hold the later pieces of a split tile
-            int pieces = 0;
-            if (finish_split)
-                while (cta + pieces + 1 < ncta && split_begin(cta + pieces + 1, ncta, p.total_work) < sg.w_tile_end)
-                    ++pieces;
-            // One thread waits (for the accumulator and, when finishing a split
-            // tile, for the later pieces' flags); the four warps leave or stay
-            // together: the TMEM loads below are warp-collective.
-            if (threadIdx.x == 0) {
-                int ok = wait_bounded(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns, p.ws.status,
-                                      kStatusEpilogueTimeout)
-                             ? 1
-                             : 0;
-                if (ok && finish_split) {
-                    for (int c2 = cta + 1; c2 <= cta + pieces; ++c2) {
-                        const uint64_t t0 = ptx::globaltimer();
-                        while (ptx::ld_acquire_gpu(p.ws.flags + c2) != p.epoch) {
-                            if (ptx::globaltimer() - t0 > p.timeout_ns) {
-                                *abort_flag = 1;
-                                atomicOr(p.ws.status, kStatusFlagTimeout);
-                                ok = 0;
-                                break;
-                            }
-                        }
-                        if (!ok)
-                            break;
-                    }
-                    if (ok) {
-                        // A split tile is always its finishing CTA's last
-                        // segment: every MMA has completed, no copy is pending,
-                        // so the stage ring is free. The next piece's partial
-                        // tile moves there with bulk copies (16 KiB per chunk).
-                        const int nch = (gi.n - sg.tn * BN) / 32 < BN / 32 ? (gi.n - sg.tn * BN) / 32 : BN / 32;
-                        const char *src = reinterpret_cast<const char *>(p.ws.partials) +
-                                          (size_t)(cta + 1) * kPartialSlotBytes;
-                        ptx::mbar_arrive_expect_tx(partial_bar, (uint32_t)nch * 8 * kBlockM * 16);
-                        for (int cc = 0; cc < nch; ++cc)
-                            ptx::bulk_load(smem_base + cc * 8 * kBlockM * 16, src + (size_t)cc * 8 * kBlockM * 16,
-                                           8 * kBlockM * 16, partial_bar, ptx::l2_policy_evict_first());
-                        ok = wait_bounded(partial_bar, 0, abort_flag, p.timeout_ns, p.ws.status,
-                                          kStatusFlagTimeout)
-                                 ? 1
-                                 : 0;
-                    }
-                }
-                *s_epi_ok = ok;
-            }
-            ptx::named_barrier(1, 128);
-            if (!*s_epi_ok)
+        const bool have = cur.next(sg);
+        while (have) {
+            Segment nx;
+            if (!cur.next(nx))
                 break;
-            if (finish_split)
-                (void)ptx::mbar_try_wait(partial_bar, 0);  // every thread acquires the landed partial tile
-            ptx::tc_fence_after();
-            const int row = sg.tm * kBlockM + r_local;
-            const uint32_t t_row = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * C::kAccCols);
-            __half *c_base = static_cast<__half *>(gi.c);
-            uint8_t *buf = epi_stage + warp * C::kEpiStageBytes;
-            // Partial tiles: [chunk][quad q][row] of float4, so a warp's stores
-            // and loads of one (chunk, q) cover 512 contiguous bytes. When
-            // finishing a split tile, the first later piece's next chunk is
-            // loaded while the current one is converted (L2 latency hidden).
-            const int nchunks = (n - sg.tn * BN) / 32 < BN / 32 ? (n - sg.tn * BN) / 32 : BN / 32;
-            // fp16 row segment (64 B, 16 words) of chunk cc -> this warp's
-            // staging buffer, 16-byte pieces XOR-swizzled by (row / 2) % 4 so
-            // that neither the row-wise writes nor the transposed reads conflict
-            // on banks; then 4 lanes per row, each store writing 8 rows x 64 B.
-            auto store_chunk = [&](const int cc, const uint32_t (&h)[16]) {
-                const int col = sg.tn * BN + cc * 32;
-                const int sw = (lane >> 1) & 3;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4 *>(buf + lane * 64 + 16 * (j ^ sw)) =
-                        make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-                __syncwarp();
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int r = 8 * q + (lane >> 2);
-                    const int piece = lane & 3;
-                    const uint4 val = *reinterpret_cast<const uint4 *>(buf + r * 64 + 16 * (piece ^ ((r >> 1) & 3)));
-                    const int grow = sg.tm * kBlockM + warp * 32 + r;
-                    if (grow < m)
-                        *reinterpret_cast<uint4 *>(c_base + (size_t)grow * (size_t)n + col + 8 * piece) = val;
-                }
-                __syncwarp();
-            };
-            auto pack = [&](float x0, float x1) {
-                __half2 h2 = __floats2half2_rn(x0, x1);
-                return *reinterpret_cast<uint32_t *>(&h2);
-            };
-            if (cont) {
-                // later piece of a split tile: fp32 partial tile to this CTA's
-                // slot; TMEM loads run half a chunk ahead of the stores
-                float4 *dst = reinterpret_cast<float4 *>(p.ws.partials) + (size_t)cta * (kPartialSlotBytes / 16) + r_local;
-                auto put = [&](const uint32_t (&v)[16], float4 *d) {
-                    if (row < m) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            d[q * kBlockM] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                                         __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-                    }
-                };
-                uint32_t va[16], vb[16];
-                ptx::tmem_ld_32x32b_x16(t_row, va);
-#pragma unroll 1
-                for (int cc = 0; cc < nchunks; ++cc) {
-                    ptx::tmem_ld_wait();
-                    ptx::tmem_ld_32x32b_x16(t_row + cc * 32 + 16, vb);
-                    put(va, dst + (size_t)cc * 8 * kBlockM);
-                    ptx::tmem_ld_wait();
-                    if (cc + 1 < nchunks)
-                        ptx::tmem_ld_32x32b_x16(t_row + (cc + 1) * 32, va);
-                    put(vb, dst + ((size_t)cc * 8 + 4) * kBlockM);
-                }
-            } else if (finish_split) {
-                // first piece of a split tile: add the later pieces' partial
-                // tiles (the next piece's from shared memory, any further
-                // ones -- a tile spanning 3+ CTAs -- from L2)
-                const float4 *sp = reinterpret_cast<const float4 *>(smem) + r_local;
-#pragma unroll 1
-                for (int cc = 0; cc < nchunks; ++cc) {
-                    uint32_t v[32];
-                    ptx::tmem_ld_32x32b_x32(t_row + cc * 32, v);
-                    ptx::tmem_ld_wait();
-                    const float4 *part = reinterpret_cast<const float4 *>(p.ws.partials) + ((size_t)cc * 8) * kBlockM +
-                                         r_local;
-                    uint32_t h[16];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        float x0 = __uint_as_float(v[4 * q]), x1 = __uint_as_float(v[4 * q + 1]);
-                        float x2 = __uint_as_float(v[4 * q + 2]), x3 = __uint_as_float(v[4 * q + 3]);
-                        if (row < m) {
-                            const float4 cur = sp[(cc * 8 + q) * kBlockM];
-                            x0 += cur.x;
-                            x1 += cur.y;
-                            x2 += cur.z;
-                            x3 += cur.w;
-                            for (int c2 = cta + 2; c2 <= cta + pieces; ++c2) {
-                                const float4 p4 = __ldcg(part + (size_t)c2 * (kPartialSlotBytes / 16) + q * kBlockM);
-                                x0 += p4.x;
-                                x1 += p4.y;
-                                x2 += p4.z;
-                                x3 += p4.w;
-                            }
-                        }
-                        h[2 * q] = pack(x0, x1);
-                        h[2 * q + 1] = pack(x2, x3);
-                    }
-                    store_chunk(cc, h);
-                }
-            } else {
-                // whole tile: TMEM loads run half a chunk (16 columns) ahead of
-                // the conversion and stores
-                uint32_t va[16], vb[16], h[16];
-                ptx::tmem_ld_32x32b_x16(t_row, va);
-#pragma unroll 1
-                for (int cc = 0; cc < nchunks; ++cc) {
-                    ptx::tmem_ld_wait();
-                    ptx::tmem_ld_32x32b_x16(t_row + cc * 32 + 16, vb);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        h[q] = zero ? 0u : pack(__uint_as_float(va[2 * q]), __uint_as_float(va[2 * q + 1]));
-                    ptx::tmem_ld_wait();
-                    if (cc + 1 < nchunks)
-                        ptx::tmem_ld_32x32b_x16(t_row + (cc + 1) * 32, va);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        h[8 + q] = zero ? 0u : pack(__uint_as_float(vb[2 * q]), __uint_as_float(vb[2 * q + 1]));
-                    store_chunk(cc, h);
-                }
+            const GInfo gi = group_info<BN>(p.groups[sg.g]);
+            // a first piece of a split tile is always a CTA's last segment
+            const int kind = sg.kt0 > 0 ? kEpiCont : kEpiWhole;
+            // One thread waits for the accumulator; the four warps leave or
+            // stay together (the TMEM loads are warp-collective).
+            if (threadIdx.x == 0)
+                s_epi_ok[it & 1] = wait_bounded(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns, p.ws.status,
+                                                kStatusEpilogueTimeout)
+                                       ? 1
+                                       : 0;
+            ptx::named_barrier(1, 128);
+            if (!s_epi_ok[it & 1]) {
+                ok = false;
+                break;
             }
+            ptx::tc_fence_after();
+            epilogue_warp<BN, CAP>(p, sg, gi, kind, warp, lane, tmem_base + (uint32_t)(acc * C::kAccCols), 0,
+                                   tile_chunks<BN>(gi, sg), epi_stage + warp * C::kEpiStageBytes, smem, 0, 0);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 ptx::mbar_arrive(acce_bar(acc));
-            if (cont) {
+            if (kind == kEpiCont) {
                 // publish this CTA's partial tile
                 ptx::named_barrier(1, 128);
                 if (threadIdx.x == 0) {
@@ -729,6 +819,70 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             if (++acc == C::kAccStages) {
                 acc = 0;
                 acc_phase ^= 1u;
+            }
+            ++it;
+            sg = nx;
+        }
+        if (threadIdx.x == 0) {
+            s_tail->seg = sg;
+            s_tail->valid = (have && ok) ? 1 : 0;
+            s_tail->acc = acc;
+            s_tail->acc_phase = (int32_t)acc_phase;
+        }
+    }
+
+    // ---- the last segment: warps 0..7 ------------------------------------------
+    // Its MMAs are the CTA's last, so the ring holds nothing but the partial
+    // tile the producer may have prefetched; warps 4..7 stage their stores in
+    // the last 2 KiB of stages 0..3.
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    tmem_base = *tmem_slot;
+    if (warp < 8) {
+        const TailState ts = *s_tail;
+        const Segment sg = ts.seg;
+        const GInfo gi = group_info<BN>(p.groups[ts.valid ? sg.g : 0]);
+        const int kind = sg.kt0 > 0 ? kEpiCont : ((p.split && sg.kt1 < sg.ktg) ? kEpiFinish : kEpiWhole);
+        if (threadIdx.x == 0) {
+            int ok = ts.valid && wait_bounded(accf_bar(ts.acc), (uint32_t)ts.acc_phase, abort_flag, p.timeout_ns,
+                                              p.ws.status, kStatusEpilogueTimeout);
+            if (ts.part_state) {
+                // the partial-tile copies must land before the CTA exits, even
+                // after an abort
+                const uint64_t t0 = ptx::globaltimer();
+                bool landed;
+                while (!(landed = ptx::mbar_try_wait(partial_bar, 0)) && ptx::globaltimer() - t0 < p.timeout_ns) {
+                }
+                if (!landed) {
+                    *abort_flag = 1;
+                    atomicOr(p.ws.status, kStatusFlagTimeout);
+                }
+                ok = ok && landed && ts.part_ok;
+            } else if (kind == kEpiFinish) {
+                ok = 0;  // the producer gave up before copying the partial tile
+            }
+            s_epi_ok[2] = ok;
+        }
+        ptx::named_barrier(1, 256);
+        if (ts.valid && s_epi_ok[2]) {
+            if (kind == kEpiFinish)
+                (void)ptx::mbar_try_wait(partial_bar, 0);  // every thread acquires the landed partial tile
+            ptx::tc_fence_after();
+            const int nch = tile_chunks<BN>(gi, sg);
+            const int half = (nch + 1) / 2;
+            const int quarter = warp & 3;
+            uint8_t *buf = warp < 4 ? epi_stage + warp * C::kEpiStageBytes
+                                    : smem + (warp - 4) * C::kStageBytes + C::kStageBytes - C::kEpiStageBytes;
+            epilogue_warp<BN, CAP>(p, sg, gi, kind, quarter, lane, tmem_base + (uint32_t)(ts.acc * C::kAccCols),
+                                   warp < 4 ? 0 : half, warp < 4 ? half : nch, buf, smem, ts.part_stage0,
+                                   ts.pieces);
+            if (kind == kEpiCont) {
+                ptx::named_barrier(1, 256);
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    ptx::st_release_gpu(p.ws.flags + blockIdx.x, p.epoch);
+                }
             }
         }
     }
