@@ -85,6 +85,45 @@ int nvfp4_grouped_gemm(int group_count, const nvfp4_problem_size *problem_sizes,
                        const void *const *SFA, const void *const *SFB,
                        void *const *C, nvfp4_stream_t stream);
 
+/*
+ * nvfp4_grouped_gemm_device -- nvfp4_grouped_gemm with the group table in
+ * DEVICE memory, so that the sizes and pointers can come from an earlier
+ * kernel (a mixture-of-experts router) without a host round trip, and so that
+ * a CUDA graph captured once can be replayed with new sizes and pointers.
+ * The submissions build problem_sizes and the pointer lists on the host and
+ * copy them to the device before each launch (submission 506336, host code
+ * that prepares the grouped launch); here the kernel reads the caller's
+ * arrays directly.
+ *
+ *   group_count      HOST int, 0 <= group_count <= NVFP4_MAX_GROUPS: number of
+ *                    entries of every array (entries may describe empty
+ *                    groups, e.g. (0, 0, 0, 1) for an expert with no tokens).
+ *   problem_sizes    DEVICE array of group_count nvfp4_problem_size, 16-byte
+ *                    aligned.
+ *   A, B, SFA, SFB, C  DEVICE arrays of group_count DEVICE addresses (8-byte
+ *                    aligned arrays), same element layouts as
+ *                    nvfp4_grouped_gemm.
+ * The arrays are read by the kernel when it runs (in stream order), not when
+ * the call returns; they must stay valid and unchanged until then.
+ * Group rules are those of nvfp4_grouped_gemm plus m, n, k <= 2^24; they are
+ * checked on the device: a group that breaks one is skipped (its C is not
+ * written), the rest of the call completes, and the next nvfp4_device_status
+ * on the stream reports NVFP4_ERR_INVALID_ARG. Only the host arguments are
+ * checked before anything is enqueued (group_count range, null or misaligned
+ * arrays).
+ * Every call rewrites the TMA descriptors of all group_count entries and
+ * launches one CTA per SM; the kernel derives the tile schedule itself.
+ * Graph capture: the workspace of (device, stream) is allocated by the first
+ * call on that pair, so make one call on the capturing stream before the
+ * capture begins; the captured launch may then be replayed any number of
+ * times (the arrays' contents may change between replays; their addresses
+ * and group_count are fixed by the capture).
+ */
+int nvfp4_grouped_gemm_device(int group_count, const nvfp4_problem_size *problem_sizes,
+                              const void *const *A, const void *const *B,
+                              const void *const *SFA, const void *const *SFB,
+                              void *const *C, nvfp4_stream_t stream);
+
 /* Largest group_count accepted by nvfp4_grouped_gemm_noalloc. */
 #define NVFP4_NOALLOC_MAX_GROUPS 64
 
@@ -120,8 +159,9 @@ int nvfp4_grouped_gemm_noalloc(int group_count, const nvfp4_problem_size *proble
 
 /*
  * nvfp4_set_tile_n -- choose the BLOCK_N of the GEMM tile for later calls in
- * this process: 128 or 256, or 0 to restore the automatic choice (128, or
- * the NVFP4_TILE_N environment variable). Results do not depend on it.
+ * this process: 128 or 256, or 0 to restore the automatic choice (256, or
+ * 128 if the NVFP4_TILE_N environment variable says so). Results do not
+ * depend on it.
  * Returns NVFP4_OK or NVFP4_ERR_INVALID_ARG.
  */
 int nvfp4_set_tile_n(int block_n);
@@ -146,8 +186,10 @@ int nvfp4_pack_scales(const void *sf_rowmajor, int rows, int k, void *sf_atoms,
 /*
  * nvfp4_device_status -- read and clear the device-side status word of the
  * (current device, stream) workspace. Synchronises `stream`. *status receives
- * NVFP4_OK, or NVFP4_ERR_TIMEOUT if a kernel of an earlier call gave up a
- * bounded wait (its C is then incomplete). Returns NVFP4_OK or NVFP4_ERR_CUDA.
+ * NVFP4_OK; NVFP4_ERR_TIMEOUT if a kernel of an earlier call gave up a
+ * bounded wait (its C is then incomplete); or NVFP4_ERR_INVALID_ARG if an
+ * nvfp4_grouped_gemm_device call skipped a group that breaks the group rules.
+ * Returns NVFP4_OK or NVFP4_ERR_CUDA.
  */
 int nvfp4_device_status(nvfp4_stream_t stream, int *status);
 

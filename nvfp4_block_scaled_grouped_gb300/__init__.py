@@ -9,6 +9,8 @@ The functions mirror the C entry points:
 
 * :func:`grouped_gemm` -- ``nvfp4_grouped_gemm`` (raw device pointers);
 * :func:`grouped_gemm_tensors` -- the same call taking torch CUDA tensors;
+* :func:`grouped_gemm_device` / :class:`DeviceGroupTable` --
+  ``nvfp4_grouped_gemm_device`` (group table in device memory);
 * :func:`pack_scales` / :func:`scale_bytes` -- the scale-layout packer;
 * :func:`device_status`, :func:`set_tile_n`.
 """
@@ -19,7 +21,8 @@ import threading
 from pathlib import Path
 
 __all__ = [
-    "Nvfp4Error", "lib", "library_path", "grouped_gemm", "grouped_gemm_tensors", "pack_scales",
+    "Nvfp4Error", "lib", "library_path", "grouped_gemm", "grouped_gemm_tensors", "grouped_gemm_device",
+    "DeviceGroupTable", "pack_scales",
     "pack_scales_tensor", "scale_bytes", "device_status", "set_tile_n", "MAX_GROUPS", "STATUS",
 ]
 
@@ -61,6 +64,8 @@ def lib() -> ctypes.CDLL:
         vp, vpp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)
         L.nvfp4_grouped_gemm.restype = ctypes.c_int
         L.nvfp4_grouped_gemm.argtypes = [ctypes.c_int, ctypes.POINTER(ProblemSize), vpp, vpp, vpp, vpp, vpp, vp]
+        L.nvfp4_grouped_gemm_device.restype = ctypes.c_int
+        L.nvfp4_grouped_gemm_device.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, vp, vp]
         L.nvfp4_scale_bytes.restype = ctypes.c_size_t
         L.nvfp4_scale_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
         L.nvfp4_pack_scales.restype = ctypes.c_int
@@ -122,6 +127,50 @@ def grouped_gemm_tensors(problem_sizes, A, B, SFA, SFB, C, stream=None) -> None:
     atom-layout buffers, C float16 [m, n] (written in place)."""
     grouped_gemm(problem_sizes, [_dptr(t) for t in A], [_dptr(t) for t in B], [_dptr(t) for t in SFA],
                  [_dptr(t) for t in SFB], [_dptr(t) for t in C], stream)
+
+
+def grouped_gemm_device(group_count: int, sizes_ptr: int, A_ptr: int, B_ptr: int, SFA_ptr: int, SFB_ptr: int,
+                        C_ptr: int, stream=None, *, check: bool = True) -> int:
+    """nvfp4_grouped_gemm_device: every argument but group_count is the device
+    address of an array of group_count entries (sizes int32 [G, 4], the others
+    uint64 device addresses)."""
+    vp = ctypes.c_void_p
+    status = lib().nvfp4_grouped_gemm_device(
+        int(group_count), vp(int(sizes_ptr) or None), vp(int(A_ptr) or None), vp(int(B_ptr) or None),
+        vp(int(SFA_ptr) or None), vp(int(SFB_ptr) or None), vp(int(C_ptr) or None),
+        vp(_stream_handle(stream) or None))
+    if check:
+        _check(status)
+    return status
+
+
+class DeviceGroupTable:
+    """Device-resident group table for :func:`grouped_gemm_device`: sizes int32
+    [G, 4] and five int64 arrays of device addresses, on `device`. ``set``
+    rewrites them (a host-to-device copy on the current stream); ``run``
+    issues the call. The arrays keep their addresses, so a captured ``run``
+    can be replayed after ``set``."""
+
+    def __init__(self, group_count: int, device="cuda"):
+        import torch
+        self.group_count = int(group_count)
+        self.sizes = torch.zeros((max(self.group_count, 1), 4), dtype=torch.int32, device=device)
+        self.ptrs = torch.zeros((5, max(self.group_count, 1)), dtype=torch.int64, device=device)
+
+    def set(self, problem_sizes, A, B, SFA, SFB, C) -> None:
+        """problem_sizes: (m, n, k, l) per group; A..C: torch tensors or ints (device addresses)."""
+        import torch
+        assert len(problem_sizes) == self.group_count
+        addr = lambda t: int(t) if isinstance(t, int) else _dptr(t)
+        host_sizes = torch.tensor([[int(v) for v in s] for s in problem_sizes], dtype=torch.int32)
+        host_ptrs = torch.tensor([[addr(t) for t in col] for col in (A, B, SFA, SFB, C)], dtype=torch.int64)
+        self.sizes[: self.group_count].copy_(host_sizes)
+        self.ptrs[:, : self.group_count].copy_(host_ptrs)
+
+    def run(self, stream=None, *, check: bool = True) -> int:
+        row = lambda i: self.ptrs[i].data_ptr()
+        return grouped_gemm_device(self.group_count, self.sizes.data_ptr(), row(0), row(1), row(2), row(3), row(4),
+                                   stream, check=check)
 
 
 def scale_bytes(rows: int, k: int) -> int:

@@ -48,8 +48,8 @@ struct DeviceState {
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
-// One workspace per (device, stream): base pointer, partial-tile slots and
-// the epoch of the last split call that used it.
+// One workspace per (device, stream): base pointer, per-CTA slots and what
+// its descriptor slots hold.
 struct StreamWorkspace {
     void *base = nullptr;
     int slots = 0;  // CTA slots for prefix scratch and partial tiles
@@ -119,7 +119,7 @@ int stream_workspace(int device, cudaStream_t stream, int slots, StreamWorkspace
         return NVFP4_OK;
     }
     void *p = nullptr;
-    const size_t bytes = workspace_bytes(NVFP4_MAX_GROUPS, slots, slots);
+    const size_t bytes = workspace_bytes(NVFP4_MAX_GROUPS, slots, slots, 2);
     cudaError_t e = cudaMalloc(&p, bytes);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMalloc(workspace)");
@@ -207,20 +207,36 @@ int check_groups(int group_count, int max_groups, const nvfp4_problem_size *prob
 
 int current_block_n() { return choose_block_n(); }
 
+// NVFP4_SPLIT forces the schedule: -1 if unset (automatic), else 0 or 1.
+int split_override() {
+    const char *s = std::getenv("NVFP4_SPLIT");
+    if (s && *s)
+        return std::atoi(s) != 0 ? 1 : 0;
+    return -1;
+}
+
 // Split (stream-K) schedules pay off when whole tiles leave the last wave
 // mostly idle: ceil(T / P) waves against T / P waves of work. They cost
 // partial-tile traffic and an extra epilogue per split tile, so they are used
-// only when whole tiles would waste at least ~30% of the time.
+// only when whole tiles would waste at least ~30% of the time (the kernel
+// applies the same integer rule to device-table calls).
 bool want_split(long long total_tiles, int sm_count) {
-    const char *s = std::getenv("NVFP4_SPLIT");
-    if (s && *s)
-        return std::atoi(s) != 0;
+    const int forced = split_override();
+    if (forced >= 0)
+        return forced != 0;
     const long long waves = (total_tiles + sm_count - 1) / sm_count;
-    return (double)waves >= 1.4 * (double)total_tiles / (double)sm_count;
+    return 10ll * waves * sm_count >= 14ll * total_tiles;
+}
+
+// Whether `stream` is capturing into a CUDA graph (the launch is then
+// replayed later, possibly after other calls changed the descriptor slots).
+bool capturing(cudaStream_t stream) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    return cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone;
 }
 
 int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles, int block_n, void *ws_base,
-                        int capacity, int prefix_slots, int partial_slots, WorkspaceState *state,
+                        int capacity, int prefix_slots, int partial_slots, int regions, WorkspaceState *state,
                         cudaStream_t stream) {
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
@@ -240,9 +256,10 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
     DeviceState *st = nullptr;
     GemmLaunch cfg;
     int desc_maps = 0;
+    const bool graph = capturing(stream);
     // One lock over set-up, launch and bookkeeping: calls that share a
-    // workspace must reach the GPU in the order their descriptor counts and
-    // cache updates were taken.
+    // workspace must reach the GPU in the order their descriptor-cache
+    // updates were taken.
     std::lock_guard<std::mutex> lock(g_mutex);
     {
         int s = device_state(device, ws_base, &st);
@@ -250,20 +267,20 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
             return s;
         const int sms = st->sm_count;
         cfg.split = (partial_slots >= sms && want_split(total_tiles, sms)) ? 1 : 0;
-        if (cfg.split) {
+        if (cfg.split)
             cfg.grid = (int)(total_work < sms ? total_work : sms);
-            cfg.epoch = ++state->epoch;
-        } else {
+        else
             cfg.grid = (int)(total_tiles < sms ? total_tiles : sms);
-            cfg.epoch = 0;
-        }
         if (group_count > kMediumGroups && prefix_slots < cfg.grid)
             return fail(NVFP4_ERR_UNSUPPORTED, "workspace has %d CTA slots, the launch needs %d", prefix_slots,
                         cfg.grid);
-        // Descriptors to patch: those whose slot does not already hold this
-        // group's pointer and shape (the slots are written only by this
-        // workspace's calls, in stream order).
-        if (state->descs.size() < 2 * (size_t)capacity)
+        // Descriptors to patch: those whose region-0 slot does not already
+        // hold this group's pointer and shape (region 0 is written only by
+        // this workspace's eager calls, in stream order). A captured launch
+        // runs whenever it is replayed: it uses region 1 (when the workspace
+        // has one, else region 0 with the cache dropped) and patches every
+        // slot it uses.
+        if (state->descs.size() < 2 * (size_t)capacity || (graph && regions < 2))
             state->descs.assign(2 * (size_t)capacity, DescKey());
         desc_maps = 0;
         for (int g = 0; g < group_count; ++g) {
@@ -272,32 +289,34 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
             if (a.m <= 0 || a.n <= 0 || a.k <= 0)
                 continue;
             const DescKey ka{a.a, a.m, a.k, kBlockM}, kb{a.b, a.n, a.k, block_n};
-            if (!(state->descs[2 * g] == ka)) {
+            if (graph || !(state->descs[2 * g] == ka)) {
                 a.patch |= 1;
                 ++desc_maps;
             }
-            if (!(state->descs[2 * g + 1] == kb)) {
+            if (graph || !(state->descs[2 * g + 1] == kb)) {
                 a.patch |= 2;
                 ++desc_maps;
             }
         }
-        cfg.desc_base = state->desc_count;
-        state->desc_count += (uint32_t)desc_maps;
     }
     cfg.block_n = block_n;
     cfg.group_count = group_count;
     cfg.desc_maps = desc_maps;
     cfg.total_tiles = (int)total_tiles;
     cfg.total_work = (int)total_work;
+    cfg.capacity = capacity;
     cfg.timeout_ns = watchdog_ns();
-    const WorkspaceView ws = workspace_view(ws_base, capacity, prefix_slots, partial_slots);
+    cfg.device_table = false;
+    cfg.dt = DeviceTable{};
+    WorkspaceView ws = workspace_view(ws_base, capacity, prefix_slots, partial_slots, regions);
+    if (graph && regions > 1)
+        ws = second_region(ws);
     const void *tmpl_b = block_n == 256 ? (const void *)&st->tmpl_b256 : (const void *)&st->tmpl_b128;
     e = launch_grouped(cfg, args, ws, &st->tmpl_a, tmpl_b, stream);
-    if (e != cudaSuccess) {
-        // nothing ran: the device counter did not move, no slot was written
-        state->desc_count -= (uint32_t)desc_maps;
-        return cuda_fail(e, "grouped GEMM launch");
-    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "grouped GEMM launch");  // nothing ran, no slot was written
+    if (graph)
+        return NVFP4_OK;
     for (int g = 0; g < group_count; ++g) {
         const GroupArgs &a = args[g];
         if (a.patch & 1)
@@ -305,6 +324,38 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
         if (a.patch & 2)
             state->descs[2 * g + 1] = DescKey{a.b, a.n, a.k, block_n};
     }
+    return NVFP4_OK;
+}
+
+int launch_device_table(int group_count, const DeviceTable &dt, int block_n, void *ws_base, int capacity,
+                        int slots, WorkspaceState *state, cudaStream_t stream) {
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState *st = nullptr;
+    int s = device_state(device, ws_base, &st);
+    if (s != NVFP4_OK)
+        return s;
+    GemmLaunch cfg;
+    cfg.block_n = block_n;
+    cfg.group_count = group_count;
+    cfg.desc_maps = 2 * group_count;  // every group's slots are rewritten
+    cfg.total_tiles = 0;              // derived by the kernel
+    cfg.total_work = 0;
+    cfg.grid = st->sm_count < slots ? st->sm_count : slots;
+    cfg.split = split_override();
+    cfg.capacity = capacity;
+    cfg.timeout_ns = watchdog_ns();
+    cfg.device_table = true;
+    cfg.dt = dt;
+    (void)state;  // region 0 and its host cache are left alone
+    const WorkspaceView ws = second_region(workspace_view(ws_base, capacity, slots, slots, 2));
+    const void *tmpl_b = block_n == 256 ? (const void *)&st->tmpl_b256 : (const void *)&st->tmpl_b128;
+    e = launch_grouped(cfg, nullptr, ws, &st->tmpl_a, tmpl_b, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "grouped GEMM launch");
     return NVFP4_OK;
 }
 
@@ -366,8 +417,45 @@ int nvfp4_grouped_gemm(int group_count, const nvfp4_problem_size *problem_sizes,
         if (s != NVFP4_OK)
             return s;
     }
-    return launch_on_workspace(group_count, args, total, block_n, w->base, NVFP4_MAX_GROUPS, w->slots, w->slots,
+    return launch_on_workspace(group_count, args, total, block_n, w->base, NVFP4_MAX_GROUPS, w->slots, w->slots, 2,
                                &w->state, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int nvfp4_grouped_gemm_device(int group_count, const nvfp4_problem_size *problem_sizes, const void *const *A,
+                              const void *const *B, const void *const *SFA, const void *const *SFB, void *const *C,
+                              nvfp4_stream_t stream) {
+    if (group_count < 0)
+        return fail(NVFP4_ERR_INVALID_ARG, "group_count %d < 0", group_count);
+    if (group_count == 0)
+        return NVFP4_OK;
+    if (group_count > NVFP4_MAX_GROUPS)
+        return fail(NVFP4_ERR_INVALID_ARG, "group_count %d > %d", group_count, NVFP4_MAX_GROUPS);
+    if (!problem_sizes || !A || !B || !SFA || !SFB || !C)
+        return fail(NVFP4_ERR_INVALID_ARG, "null problem_sizes or pointer array");
+    if (!aligned16(problem_sizes))
+        return fail(NVFP4_ERR_MISALIGNED, "problem_sizes not 16-byte aligned");
+    const void *arrays[5] = {A, B, SFA, SFB, C};
+    for (const void *q : arrays)
+        if ((reinterpret_cast<uintptr_t>(q) & 7u) != 0)
+            return fail(NVFP4_ERR_MISALIGNED, "pointer array not 8-byte aligned");
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    StreamWorkspace *w = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        int s = stream_workspace(device, reinterpret_cast<cudaStream_t>(stream), sms, &w);
+        if (s != NVFP4_OK)
+            return s;
+    }
+    const DeviceTable dt{problem_sizes, A, B, SFA, SFB, C};
+    return launch_device_table(group_count, dt, choose_block_n(), w->base, NVFP4_MAX_GROUPS, w->slots, &w->state,
+                               reinterpret_cast<cudaStream_t>(stream));
 }
 
 int nvfp4_pack_scales(const void *sf_rowmajor, int rows, int k, void *sf_atoms, nvfp4_stream_t stream) {
@@ -417,9 +505,14 @@ int nvfp4_device_status(nvfp4_stream_t stream, int *status) {
     }
     if (e != cudaSuccess)
         return cuda_fail(e, "reading the device status word");
-    if (word != 0) {
+    if (word & kStatusTimeoutMask) {
         *status = NVFP4_ERR_TIMEOUT;
-        fail(NVFP4_ERR_TIMEOUT, "a bounded wait gave up (status bits 0x%x: 1 producer, 2 MMA, 4 epilogue)", word);
+        fail(NVFP4_ERR_TIMEOUT,
+             "a bounded wait gave up (status bits 0x%x: 1 producer, 2 MMA, 4 epilogue, 8 partial tile, 16 descriptors)",
+             word);
+    } else if (word & kStatusBadGroup) {
+        *status = NVFP4_ERR_INVALID_ARG;
+        fail(NVFP4_ERR_INVALID_ARG, "a device-table call skipped a group that breaks the group rules");
     }
     return NVFP4_OK;
 }

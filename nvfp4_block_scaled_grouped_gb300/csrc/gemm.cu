@@ -102,16 +102,59 @@ struct Cfg {
     static constexpr uint32_t kIdesc = ptx::idesc_mxf4nvf4(kBlockM, BN);
 };
 
-template <int CAP>
+// DEV: the group table is the caller's device arrays (`dt`), else `groups`.
+template <int CAP, bool DEV>
 struct GemmParams {
     alignas(64) uint8_t tmpl_a[128];
     alignas(64) uint8_t tmpl_b[128];
     WorkspaceView ws;
+    DeviceTable dt;
     int32_t group_count, block_n, total_tiles, total_work, split, desc_maps;
-    uint32_t epoch, desc_base;
     uint64_t timeout_ns;
-    GroupArgs groups[CAP];
+    GroupArgs groups[DEV ? 1 : CAP];
 };
+
+__device__ __forceinline__ bool aligned16(const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
+
+// Largest m, n or k of a device-table group (keeps every tile and unit count
+// of a call inside int32).
+constexpr int kDeviceTableMaxDim = 1 << 24;
+
+// Group g's arguments: the kernel parameter's entry, or the caller's device
+// arrays checked against the same rules as the host entry point; a group that
+// breaks one is skipped (sizes read as 0) and *bad is set.
+template <int CAP, bool DEV>
+__device__ __forceinline__ GroupArgs load_group(const GemmParams<CAP, DEV> &p, int g, bool *bad = nullptr) {
+    if constexpr (!DEV) {
+        return p.groups[g];
+    } else {
+        const int4 sz = __ldg(reinterpret_cast<const int4 *>(p.dt.sizes) + g);
+        GroupArgs a;
+        a.m = sz.x;
+        a.n = sz.y;
+        a.k = sz.z;
+        a.patch = 3;
+        a.a = p.dt.a[g];
+        a.b = p.dt.b[g];
+        a.sfa = p.dt.sfa[g];
+        a.sfb = p.dt.sfb[g];
+        a.c = p.dt.c[g];
+        bool ok = a.m >= 0 && a.n >= 0 && a.k >= 0 && sz.w >= 0 && a.m <= kDeviceTableMaxDim &&
+                  a.n <= kDeviceTableMaxDim && a.k <= kDeviceTableMaxDim;
+        if (ok && a.m > 0 && a.n > 0) {
+            ok = sz.w == 1 && a.k % 32 == 0 && a.n % 32 == 0 && a.c && aligned16(a.c);
+            if (ok && a.k > 0)
+                ok = a.a && a.b && a.sfa && a.sfb && aligned16(a.a) && aligned16(a.b) && aligned16(a.sfa) &&
+                     aligned16(a.sfb);
+        }
+        if (!ok) {
+            if (bad)
+                *bad = true;
+            a.m = a.n = a.k = 0;
+        }
+        return a;
+    }
+}
 
 __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
 
@@ -202,16 +245,24 @@ struct Segment {
     int w_tile_end;  // schedule index one past the tile's last unit
 };
 
+// Whether a split schedule pays for T tiles on P CTAs: whole tiles would take
+// ceil(T / P) waves for T / P waves of work, and 1.4x is the break-even point
+// (the host applies the same integer rule).
+__device__ __forceinline__ bool split_pays(int T, int P) {
+    const long long waves = (T + P - 1) / P;
+    return 10ll * waves * P >= 14ll * T;
+}
+
 // First schedule unit of CTA c out of p in a split (stream-K) schedule.
 __device__ __forceinline__ int split_begin(int c, int p, int total_work) {
     return (int)(((long long)c * total_work) / p);
 }
 
 // The sequence of segments one CTA processes; every role walks the same one.
-template <int BN>
+template <int BN, int CAP, bool DEV>
 struct Cursor {
     const int32_t *prefix, *wprefix;
-    const GroupArgs *groups;
+    const GemmParams<CAP, DEV> *prm;
     int group_count, split;
     int w, w_end;                 // split schedule: contiguous schedule units
     int tile, total_tiles, step;  // whole-tile schedule: round-robin tiles
@@ -222,7 +273,7 @@ struct Cursor {
             if (w >= w_end)
                 return false;
             s.g = find_group(wprefix, group_count, w);
-            const GInfo gi = group_info<BN>(groups[s.g]);
+            const GInfo gi = group_info<BN>(load_group(*prm, s.g));
             const int local = w - wprefix[s.g];
             t = local / gi.work_tiles;
             s.ktg = gi.work_tiles;
@@ -236,7 +287,7 @@ struct Cursor {
             if (tile >= total_tiles)
                 return false;
             s.g = find_group(prefix, group_count, tile);
-            const GInfo gi = group_info<BN>(groups[s.g]);
+            const GInfo gi = group_info<BN>(load_group(*prm, s.g));
             t = tile - prefix[s.g];
             s.tm = t % gi.tiles_m;
             s.tn = t / gi.tiles_m;
@@ -280,8 +331,8 @@ __device__ __forceinline__ int tile_chunks(const GInfo &gi, const Segment &sg) {
 // columns) ahead of the arithmetic and stores. `buf` is the warp's 2 KiB
 // staging buffer; `smem` the CTA's ring (holding the next piece's partial tile
 // from stage part_stage0 when finishing a split tile).
-template <int BN, int CAP>
-__device__ __forceinline__ void epilogue_warp(const GemmParams<CAP> &p, const Segment &sg, const GInfo &gi,
+template <int BN, int CAP, bool DEV>
+__device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, const Segment &sg, const GInfo &gi,
                                               const int kind, const int quarter, const int lane,
                                               const uint32_t t_acc, const int c0, const int c1, uint8_t *buf,
                                               const uint8_t *smem, const int part_stage0, const int pieces) {
@@ -410,8 +461,8 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP> &p, const Se
     }
 }
 
-template <int BN, int CAP>
-__global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams<CAP> p) {
+template <int BN, int CAP, bool DEV>
+__global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams<CAP, DEV> p) {
     using C = Cfg<BN, CAP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -419,6 +470,14 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int group_count = p.group_count;
+    // descriptors are patched in this call (host table: only those that changed)
+    const bool publish = DEV || p.desc_maps != 0;
+    // Tag of this call's partial-tile flags: one more than the last completed
+    // call's on this workspace (never 0, the value of a fresh flag).
+    auto call_epoch = [&]() {
+        const uint32_t e = *reinterpret_cast<const volatile uint32_t *>(p.ws.epoch) + 1u;
+        return e ? e : 1u;
+    };
 
     uint8_t *bar_area = smem + C::kStages * C::kStageBytes;
     const uint32_t bars = ptx::smem_addr(bar_area);
@@ -465,7 +524,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         // Patch the descriptors of this CTA's share of the groups.
         uint32_t patched = 0;
         for (int g = blockIdx.x + lane * gridDim.x; g < group_count; g += 32 * gridDim.x) {
-            const GroupArgs &a = p.groups[g];
+            const GroupArgs a = load_group(p, g);
             if (a.m <= 0 || a.n <= 0 || a.k <= 0)
                 continue;
             const uint32_t row_bytes = (uint32_t)(a.k / 2);
@@ -483,10 +542,13 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 ++patched;
             }
         }
-        if (patched) {
+        // Publication: every CTA adds 1 once its lanes' descriptors are
+        // released; producers wait for all gridDim.x.
+        if (patched)
             ptx::tmap_release();
-            ptx::red_release_add_gpu(p.ws.desc_count, patched);
-        }
+        __syncwarp();
+        if (publish && lane == 0)
+            ptx::red_release_add_gpu(p.ws.desc_count, 1u);
         // The producer needs the barriers and the prefix sums, not TMEM: it
         // starts once warp 6 has the prefix sums, while the TMEM allocation
         // may still be in progress.
@@ -498,25 +560,72 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         ptx::tmem_relinquish();
     } else if (warp == 6) {
         // Exclusive prefix sums of output tiles and schedule units per group.
-        // The group table lives in the constant bank, where a warp reading
-        // different addresses is serialised, so every lane walks all groups
-        // with the same index (broadcast reads) and lane g % 32 stores entry g.
-        int bt = 0, bw = 0;
-#pragma unroll 4
-        for (int g = 0; g < group_count; ++g) {
-            const GroupArgs &a = p.groups[g];
-            const int tiles = (a.m > 0 && a.n > 0) ? ceil_div_i(a.m, kBlockM) * ceil_div_i(a.n, BN) : 0;
-            const int kt = ceil_div_i(a.k, kBlockK);
-            if (lane == (g & 31)) {
-                prefix[g] = bt;
-                wprefix[g] = bw;
+        if constexpr (DEV) {
+            // The caller's table in global memory: 32 groups per step, one per
+            // lane (independent loads), then a warp scan. A call whose unit
+            // count overflows int32 does nothing and is reported.
+            const unsigned full = 0xffffffffu;
+            long long bt = 0, bw = 0;
+            bool bad = false;
+            for (int g0 = 0; g0 < group_count; g0 += 32) {
+                const int g = g0 + lane;
+                long long t = 0, w = 0;
+                if (g < group_count) {
+                    const GroupArgs a = load_group(p, g, &bad);
+                    t = (a.m > 0 && a.n > 0) ? (long long)ceil_div_i(a.m, kBlockM) * ceil_div_i(a.n, BN) : 0;
+                    const int kt = ceil_div_i(a.k, kBlockK);
+                    w = t * (kt > 1 ? kt : 1);
+                }
+                long long it = t, iw = w;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const long long ut = __shfl_up_sync(full, it, o), uw = __shfl_up_sync(full, iw, o);
+                    if (lane >= o) {
+                        it += ut;
+                        iw += uw;
+                    }
+                }
+                if (g < group_count) {
+                    prefix[g] = (int32_t)(bt + it - t);
+                    wprefix[g] = (int32_t)(bw + iw - w);
+                }
+                bt += __shfl_sync(full, it, 31);
+                bw += __shfl_sync(full, iw, 31);
             }
-            bt += tiles;
-            bw += tiles * (kt > 1 ? kt : 1);
-        }
-        if (lane == 0) {
-            prefix[group_count] = bt;
-            wprefix[group_count] = bw;
+            if (bw > 0x7fffffffLL) {
+                for (int g = lane; g < group_count; g += 32)
+                    prefix[g] = wprefix[g] = 0;
+                bt = bw = 0;
+                bad = true;
+            }
+            if (lane == 0) {
+                prefix[group_count] = (int32_t)bt;
+                wprefix[group_count] = (int32_t)bw;
+            }
+            if (__any_sync(full, bad) && blockIdx.x == 0 && lane == 0)
+                atomicOr(p.ws.status, kStatusBadGroup);
+        } else {
+            // The group table lives in the constant bank, where a warp
+            // reading different addresses is serialised, so every lane walks
+            // all groups with the same index (broadcast reads) and lane g % 32
+            // stores entry g.
+            int bt = 0, bw = 0;
+#pragma unroll 4
+            for (int g = 0; g < group_count; ++g) {
+                const GroupArgs &a = p.groups[g];
+                const int tiles = (a.m > 0 && a.n > 0) ? ceil_div_i(a.m, kBlockM) * ceil_div_i(a.n, BN) : 0;
+                const int kt = ceil_div_i(a.k, kBlockK);
+                if (lane == (g & 31)) {
+                    prefix[g] = bt;
+                    wprefix[g] = bw;
+                }
+                bt += tiles;
+                bw += tiles * (kt > 1 ? kt : 1);
+            }
+            if (lane == 0) {
+                prefix[group_count] = bt;
+                wprefix[group_count] = bw;
+            }
         }
         __syncwarp();
         ptx::named_barrier_arrive(2, 64);
@@ -528,10 +637,19 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         ptx::tc_fence_after();
         tmem_base = *tmem_slot;
     }
-    const Cursor<BN> cursor0{prefix, wprefix, p.groups, group_count, p.split,
-                             split_begin(blockIdx.x, gridDim.x, p.total_work),
-                             split_begin(blockIdx.x + 1, gridDim.x, p.total_work),
-                             (int)blockIdx.x, p.total_tiles, (int)gridDim.x};
+    // Schedule of the call: given by the host, or (device table) derived here
+    // by every CTA from the same prefix sums with the host's rule. A split
+    // schedule uses the first P CTAs.
+    const int total_tiles = DEV ? prefix[group_count] : p.total_tiles;
+    const int total_work = DEV ? wprefix[group_count] : p.total_work;
+    int split = p.split;
+    if (DEV && split < 0)
+        split = (p.ws.partial_slots >= (int)gridDim.x && split_pays(total_tiles, (int)gridDim.x)) ? 1 : 0;
+    const int P = split ? (total_work < (int)gridDim.x ? total_work : (int)gridDim.x) : (int)gridDim.x;
+    const Cursor<BN, CAP, DEV> cursor0{prefix, wprefix, &p, group_count, split,
+                                       (int)blockIdx.x < P ? split_begin(blockIdx.x, P, total_work) : 0,
+                                       (int)blockIdx.x < P ? split_begin(blockIdx.x + 1, P, total_work) : 0,
+                                       (int)blockIdx.x, total_tiles, (int)gridDim.x};
 
     if (warp == 4) {
         // ===================== TMA producer =====================
@@ -542,14 +660,14 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
             int prev_g = -1;
-            bool descs_ready = p.desc_maps == 0;
+            bool descs_ready = !publish;
             bool ok = true;
-            Cursor<BN> cur = cursor0;
+            Cursor<BN, CAP, DEV> cur = cursor0;
             Segment sg;
             bool any = false;
             while (ok && cur.next(sg)) {
                 any = true;
-                const GInfo gi = group_info<BN>(p.groups[sg.g]);
+                const GInfo gi = group_info<BN>(load_group(p, sg.g));
                 const int k_tiles = gi.k_tiles;
                 const int kend = sg.kt1 < k_tiles ? sg.kt1 : k_tiles;
                 if (sg.kt0 >= kend)
@@ -559,8 +677,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 const uint8_t *tmap_b = tmap_a + 128;
                 if (!descs_ready) {
                     // every group's descriptors are patched by some CTA at start-up
-                    if (!wait_counter(p.ws.desc_count, p.desc_base + (uint32_t)p.desc_maps, abort_flag,
-                                      p.timeout_ns, p.ws.status)) {
+                    if (!wait_counter(p.ws.desc_count, gridDim.x, abort_flag, p.timeout_ns, p.ws.status)) {
                         ok = false;
                         break;
                     }
@@ -601,20 +718,21 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                     }
                 }
             }
-            if (ok && any && p.split && sg.kt0 == 0 && sg.kt1 < sg.ktg && !*abort_flag) {
+            if (ok && any && split && sg.kt0 == 0 && sg.kt1 < sg.ktg && !*abort_flag) {
                 // The last segment is the first piece of a split tile. Once the
                 // later pieces are published (they are their CTAs' first
                 // segments, so usually long before), the next piece's partial
                 // tile is copied into the ring, each stage as soon as the MMAs
                 // reading it have completed, oldest stage first.
-                const int cta = blockIdx.x, ncta = gridDim.x;
+                const int cta = blockIdx.x;
+                const uint32_t epoch = call_epoch();
                 int pieces = 0;
-                while (cta + pieces + 1 < ncta && split_begin(cta + pieces + 1, ncta, p.total_work) < sg.w_tile_end)
+                while (cta + pieces + 1 < P && split_begin(cta + pieces + 1, P, total_work) < sg.w_tile_end)
                     ++pieces;
                 bool flags_ok = true;
                 for (int c2 = cta + 1; c2 <= cta + pieces && flags_ok; ++c2) {
                     const uint64_t t0 = ptx::globaltimer();
-                    while (ptx::ld_acquire_gpu(p.ws.flags + c2) != p.epoch) {
+                    while (ptx::ld_acquire_gpu(p.ws.flags + c2) != epoch) {
                         if (*abort_flag) {
                             flags_ok = false;
                             break;
@@ -630,7 +748,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 s_tail->pieces = pieces;
                 if (flags_ok) {
                     ptx::fence_proxy_async_global();
-                    const int nch = tile_chunks<BN>(group_info<BN>(p.groups[sg.g]), sg);
+                    const int nch = tile_chunks<BN>(group_info<BN>(load_group(p, sg.g)), sg);
                     const char *src =
                         reinterpret_cast<const char *>(p.ws.partials) + (size_t)(cta + 1) * kPartialSlotBytes;
                     bool good = true;
@@ -672,10 +790,10 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            Cursor<BN> cur = cursor0;
+            Cursor<BN, CAP, DEV> cur = cursor0;
             Segment sg;
             while (ok && cur.next(sg)) {
-                const GInfo gi = group_info<BN>(p.groups[sg.g]);
+                const GInfo gi = group_info<BN>(load_group(p, sg.g));
                 const int k_tiles = gi.k_tiles;
                 const int k_blocks = gi.k_blocks;
                 const int kend = sg.kt1 < k_tiles ? sg.kt1 : k_tiles;
@@ -727,10 +845,10 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        Cursor<BN> cur = cursor0;
+        Cursor<BN, CAP, DEV> cur = cursor0;
         Segment sg;
         while (ok && cur.next(sg)) {
-            const GInfo gi = group_info<BN>(p.groups[sg.g]);
+            const GInfo gi = group_info<BN>(load_group(p, sg.g));
             const int k_tiles = gi.k_tiles;
             const int k_blocks = gi.k_blocks;
             const int kend = sg.kt1 < k_tiles ? sg.kt1 : k_tiles;
@@ -779,14 +897,14 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         int acc = 0, it = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        Cursor<BN> cur = cursor0;
+        Cursor<BN, CAP, DEV> cur = cursor0;
         Segment sg;
         const bool have = cur.next(sg);
         while (have) {
             Segment nx;
             if (!cur.next(nx))
                 break;
-            const GInfo gi = group_info<BN>(p.groups[sg.g]);
+            const GInfo gi = group_info<BN>(load_group(p, sg.g));
             // a first piece of a split tile is always a CTA's last segment
             const int kind = sg.kt0 > 0 ? kEpiCont : kEpiWhole;
             // One thread waits for the accumulator; the four warps leave or
@@ -802,7 +920,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 break;
             }
             ptx::tc_fence_after();
-            epilogue_warp<BN, CAP>(p, sg, gi, kind, warp, lane, tmem_base + (uint32_t)(acc * C::kAccCols), 0,
+            epilogue_warp<BN, CAP, DEV>(p, sg, gi, kind, warp, lane, tmem_base + (uint32_t)(acc * C::kAccCols), 0,
                                    tile_chunks<BN>(gi, sg), epi_stage + warp * C::kEpiStageBytes, smem, 0, 0);
             ptx::tc_fence_before();
             __syncwarp();
@@ -813,7 +931,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 ptx::named_barrier(1, 128);
                 if (threadIdx.x == 0) {
                     __threadfence();
-                    ptx::st_release_gpu(p.ws.flags + cta, p.epoch);
+                    ptx::st_release_gpu(p.ws.flags + cta, call_epoch());
                 }
             }
             if (++acc == C::kAccStages) {
@@ -842,8 +960,8 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     if (warp < 8) {
         const TailState ts = *s_tail;
         const Segment sg = ts.seg;
-        const GInfo gi = group_info<BN>(p.groups[ts.valid ? sg.g : 0]);
-        const int kind = sg.kt0 > 0 ? kEpiCont : ((p.split && sg.kt1 < sg.ktg) ? kEpiFinish : kEpiWhole);
+        const GInfo gi = group_info<BN>(load_group(p, ts.valid ? sg.g : 0));
+        const int kind = sg.kt0 > 0 ? kEpiCont : ((split && sg.kt1 < sg.ktg) ? kEpiFinish : kEpiWhole);
         if (threadIdx.x == 0) {
             int ok = ts.valid && wait_bounded(accf_bar(ts.acc), (uint32_t)ts.acc_phase, abort_flag, p.timeout_ns,
                                               p.ws.status, kStatusEpilogueTimeout);
@@ -874,14 +992,14 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             const int quarter = warp & 3;
             uint8_t *buf = warp < 4 ? epi_stage + warp * C::kEpiStageBytes
                                     : smem + (warp - 4) * C::kStageBytes + C::kStageBytes - C::kEpiStageBytes;
-            epilogue_warp<BN, CAP>(p, sg, gi, kind, quarter, lane, tmem_base + (uint32_t)(ts.acc * C::kAccCols),
+            epilogue_warp<BN, CAP, DEV>(p, sg, gi, kind, quarter, lane, tmem_base + (uint32_t)(ts.acc * C::kAccCols),
                                    warp < 4 ? 0 : half, warp < 4 ? half : nch, buf, smem, ts.part_stage0,
                                    ts.pieces);
             if (kind == kEpiCont) {
                 ptx::named_barrier(1, 256);
                 if (threadIdx.x == 0) {
                     __threadfence();
-                    ptx::st_release_gpu(p.ws.flags + blockIdx.x, p.epoch);
+                    ptx::st_release_gpu(p.ws.flags + blockIdx.x, call_epoch());
                 }
             }
         }
@@ -894,13 +1012,20 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, C::kTmemCols);
     }
+    // The last CTA to finish (every other one is past its descriptor wait and
+    // its flag traffic) resets the call counters and records the epoch.
+    if (threadIdx.x == 0 && atomicAdd(p.ws.done, 1u) == gridDim.x - 1) {
+        *p.ws.desc_count = 0;
+        *p.ws.done = 0;
+        *p.ws.epoch = call_epoch();
+    }
 }
 
-template <int BN, int CAP>
+template <int BN, int CAP, bool DEV>
 cudaError_t launch_cap(const GemmLaunch &cfg, const GroupArgs *groups, const WorkspaceView &ws,
                        const void *tmpl_a, const void *tmpl_b, cudaStream_t stream) {
-    static_assert(sizeof(GemmParams<CAP>) <= 32000, "kernel parameter limit");
-    GemmParams<CAP> prm;
+    static_assert(sizeof(GemmParams<CAP, DEV>) <= 32000, "kernel parameter limit");
+    GemmParams<CAP, DEV> prm;
     std::memcpy(prm.tmpl_a, tmpl_a, 128);
     std::memcpy(prm.tmpl_b, tmpl_b, 128);
     prm.ws = ws;
@@ -910,12 +1035,16 @@ cudaError_t launch_cap(const GemmLaunch &cfg, const GroupArgs *groups, const Wor
     prm.total_work = cfg.total_work;
     prm.split = cfg.split;
     prm.desc_maps = cfg.desc_maps;
-    prm.epoch = cfg.epoch;
-    prm.desc_base = cfg.desc_base;
     prm.timeout_ns = cfg.timeout_ns;
-    std::memcpy(prm.groups, groups, sizeof(GroupArgs) * (size_t)cfg.group_count);
-    if (cfg.group_count < CAP)
-        std::memset(prm.groups + cfg.group_count, 0, sizeof(GroupArgs) * (size_t)(CAP - cfg.group_count));
+    if constexpr (DEV) {
+        prm.dt = cfg.dt;
+        std::memset(prm.groups, 0, sizeof(prm.groups));
+    } else {
+        prm.dt = DeviceTable{};
+        std::memcpy(prm.groups, groups, sizeof(GroupArgs) * (size_t)cfg.group_count);
+        if (cfg.group_count < CAP)
+            std::memset(prm.groups + cfg.group_count, 0, sizeof(GroupArgs) * (size_t)(CAP - cfg.group_count));
+    }
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)cfg.grid, 1, 1);
     lc.blockDim = dim3(Cfg<BN, CAP>::kThreads, 1, 1);
@@ -926,23 +1055,27 @@ cudaError_t launch_cap(const GemmLaunch &cfg, const GroupArgs *groups, const Wor
     attr[0].val.cooperative = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    return cudaLaunchKernelEx(&lc, grouped_gemm_kernel<BN, CAP>, prm);
+    return cudaLaunchKernelEx(&lc, grouped_gemm_kernel<BN, CAP, DEV>, prm);
 }
 
 }  // namespace
 
 cudaError_t prepare_gemm_kernels(int /*device*/) {
     cudaError_t e = cudaSuccess;
-#define NVFP4_SET_SMEM(BN, CAP)                                                                             \
-    if (e == cudaSuccess)                                                                                   \
-        e = cudaFuncSetAttribute(grouped_gemm_kernel<BN, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+#define NVFP4_SET_SMEM(BN, CAP, DEV)                                                                             \
+    if (e == cudaSuccess)                                                                                        \
+        e = cudaFuncSetAttribute(grouped_gemm_kernel<BN, CAP, DEV>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                  (int)Cfg<BN, CAP>::kSmemBytes);
-    NVFP4_SET_SMEM(128, kSmallGroups)
-    NVFP4_SET_SMEM(128, kMediumGroups)
-    NVFP4_SET_SMEM(128, NVFP4_MAX_GROUPS)
-    NVFP4_SET_SMEM(256, kSmallGroups)
-    NVFP4_SET_SMEM(256, kMediumGroups)
-    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS)
+    NVFP4_SET_SMEM(128, kSmallGroups, false)
+    NVFP4_SET_SMEM(128, kMediumGroups, false)
+    NVFP4_SET_SMEM(128, NVFP4_MAX_GROUPS, false)
+    NVFP4_SET_SMEM(256, kSmallGroups, false)
+    NVFP4_SET_SMEM(256, kMediumGroups, false)
+    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS, false)
+    NVFP4_SET_SMEM(128, kMediumGroups, true)
+    NVFP4_SET_SMEM(128, NVFP4_MAX_GROUPS, true)
+    NVFP4_SET_SMEM(256, kMediumGroups, true)
+    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS, true)
 #undef NVFP4_SET_SMEM
     return e;
 }
@@ -956,14 +1089,22 @@ cudaError_t launch_grouped(const GemmLaunch &cfg, const GroupArgs *groups, const
     if (cfg.group_count > kMediumGroups && ws.prefix_slots < cfg.grid)
         return cudaErrorInvalidValue;
     const bool wide = cfg.block_n == 256;
+    if (cfg.device_table) {
+        // shared-memory prefix sums up to kMediumGroups groups
+        if (cfg.group_count <= kMediumGroups)
+            return wide ? launch_cap<256, kMediumGroups, true>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
+                        : launch_cap<128, kMediumGroups, true>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
+        return wide ? launch_cap<256, NVFP4_MAX_GROUPS, true>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
+                    : launch_cap<128, NVFP4_MAX_GROUPS, true>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
+    }
     if (cfg.group_count <= kSmallGroups)
-        return wide ? launch_cap<256, kSmallGroups>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
-                    : launch_cap<128, kSmallGroups>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
+        return wide ? launch_cap<256, kSmallGroups, false>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
+                    : launch_cap<128, kSmallGroups, false>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
     if (cfg.group_count <= kMediumGroups)
-        return wide ? launch_cap<256, kMediumGroups>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
-                    : launch_cap<128, kMediumGroups>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
-    return wide ? launch_cap<256, NVFP4_MAX_GROUPS>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
-                : launch_cap<128, NVFP4_MAX_GROUPS>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
+        return wide ? launch_cap<256, kMediumGroups, false>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
+                    : launch_cap<128, kMediumGroups, false>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
+    return wide ? launch_cap<256, NVFP4_MAX_GROUPS, false>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
+                : launch_cap<128, NVFP4_MAX_GROUPS, false>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
 }
 
 }  // namespace nvfp4

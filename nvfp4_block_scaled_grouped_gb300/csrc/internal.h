@@ -29,6 +29,17 @@ struct GroupArgs {
     void *c;
 };
 
+// A call whose group table stays in device memory: the caller's arrays of
+// group_count sizes and pointers, read by the kernel (nothing on the host).
+struct DeviceTable {
+    const nvfp4_problem_size *sizes;
+    const void *const *a;
+    const void *const *b;
+    const void *const *sfa;
+    const void *const *sfb;
+    void *const *c;
+};
+
 // Group counts with a kernel instantiation (the parameter block holds
 // GroupArgs[CAP]); calls use the smallest that fits.
 constexpr int kSmallGroups = 8;
@@ -44,15 +55,28 @@ constexpr int kDescBytes = 128;
 __host__ __device__ constexpr size_t cta_prefix_bytes(int capacity) { return 2 * round_up(sizeof(int32_t) * (size_t)(capacity + 1), 128); }
 
 // Device workspace, carved from one allocation at 128-byte aligned offsets.
-//   header      128 B: status word (bit flags of bounded waits that gave up) at
-//               byte 0, descriptor-publication counter at byte 64
-//   tmaps       TMA descriptors [capacity][A, B], 128 B each
+//   header      128 B: status word (bit flags of bounded waits that gave up or
+//               of rejected device-table groups) at byte 0; at byte 64 the
+//               descriptor-publication counter (CTAs that have published their
+//               patched descriptors in the running call), at 96 the count of
+//               CTAs that have finished the running call, at 100 the epoch of
+//               the last completed call. The last CTA of a call to finish
+//               resets both counters and advances the epoch, so nothing on the
+//               host tracks them (calls replayed from a CUDA graph included).
+//   tmaps       TMA descriptors [regions][capacity][A, B], 128 B each. Region
+//               0 serves eager host-table calls (its contents are cached on
+//               the host); region 1, where present, serves calls whose
+//               launch may run at another time or patches slots the host
+//               cannot see: captured launches and device-table calls. Those
+//               rewrite every slot they use on every run.
 //   cta_prefix  [prefix_slots][cta_prefix_bytes(capacity)]  (capacity > 64 only)
 //   flags       uint32 [partial_slots]   epoch of the partial tile a CTA published
 //   partials    [partial_slots][128 x 256 fp32]  split-schedule partial tiles
 struct WorkspaceView {
     uint32_t *status;
     uint32_t *desc_count;
+    uint32_t *done;
+    uint32_t *epoch;
     uint8_t *tmaps;
     int32_t *cta_prefix;
     uint32_t *flags;
@@ -60,24 +84,28 @@ struct WorkspaceView {
     int32_t capacity;
     int32_t prefix_slots;
     int32_t partial_slots;
+    int32_t regions;
 };
 
-constexpr size_t workspace_bytes(int capacity, int prefix_slots = 0, int partial_slots = 0) {
-    return 128 + (size_t)kDescBytes * 2 * (size_t)capacity +
+constexpr size_t workspace_bytes(int capacity, int prefix_slots = 0, int partial_slots = 0, int regions = 1) {
+    return 128 + (size_t)kDescBytes * 2 * (size_t)capacity * (size_t)regions +
            (capacity > kMediumGroups ? cta_prefix_bytes(capacity) * (size_t)prefix_slots : 0) +
            (partial_slots > 0 ? round_up(sizeof(uint32_t) * (size_t)partial_slots, 128) +
                                     kPartialSlotBytes * (size_t)partial_slots
                               : 0);
 }
 
-inline WorkspaceView workspace_view(void *base, int capacity, int prefix_slots = 0, int partial_slots = 0) {
+inline WorkspaceView workspace_view(void *base, int capacity, int prefix_slots = 0, int partial_slots = 0,
+                                    int regions = 1) {
     uint8_t *p = static_cast<uint8_t *>(base);
     WorkspaceView v;
     v.status = reinterpret_cast<uint32_t *>(p);
     v.desc_count = reinterpret_cast<uint32_t *>(p + 64);
+    v.done = reinterpret_cast<uint32_t *>(p + 96);
+    v.epoch = reinterpret_cast<uint32_t *>(p + 100);
     p += 128;
     v.tmaps = p;
-    p += (size_t)kDescBytes * 2 * (size_t)capacity;
+    p += (size_t)kDescBytes * 2 * (size_t)capacity * (size_t)regions;
     v.cta_prefix = nullptr;
     v.prefix_slots = 0;
     if (capacity > kMediumGroups) {
@@ -94,6 +122,13 @@ inline WorkspaceView workspace_view(void *base, int capacity, int prefix_slots =
     }
     v.capacity = capacity;
     v.partial_slots = partial_slots;
+    v.regions = regions;
+    return v;
+}
+
+// The same workspace with descriptor region 1 in place of region 0.
+inline WorkspaceView second_region(WorkspaceView v) {
+    v.tmaps += (size_t)kDescBytes * 2 * (size_t)v.capacity;
     return v;
 }
 
@@ -103,19 +138,23 @@ constexpr uint32_t kStatusMmaTimeout = 2u;
 constexpr uint32_t kStatusEpilogueTimeout = 4u;
 constexpr uint32_t kStatusFlagTimeout = 8u;
 constexpr uint32_t kStatusDescTimeout = 16u;
+constexpr uint32_t kStatusBadGroup = 32u;  // a device-table group failed validation and was skipped
+constexpr uint32_t kStatusTimeoutMask = 31u;
 
 // Launch configuration chosen by the host for one call.
 struct GemmLaunch {
     int block_n;            // 128 or 256
     int group_count;
     int desc_maps;          // descriptors the kernel patches (bits set in GroupArgs::patch)
-    int total_tiles;        // output tiles
-    int total_work;         // schedule units: sum over tiles of max(k-tiles, 1)
+    int total_tiles;        // output tiles (host-table calls)
+    int total_work;         // schedule units: sum over tiles of max(k-tiles, 1) (host-table calls)
     int grid;               // persistent CTAs (all resident: cooperative launch)
-    int split;              // 1: CTAs take equal ranges of schedule units (tiles may be split along K)
-    uint32_t epoch;         // tag of this call's partial-tile flags (split schedules)
-    uint32_t desc_base;     // descriptor counter value before this call
+    int split;              // 1: CTAs take equal ranges of schedule units (tiles may be split along K);
+                            // device-table calls: -1 = decided by the kernel, else forced
+    int capacity;           // workspace descriptor capacity (groups)
     uint64_t timeout_ns;    // bound of every wait
+    bool device_table;      // the group table is `dt` (device memory), not the host array
+    DeviceTable dt;
 };
 
 // Host launcher (gemm.cu). `tmpl_a` / `tmpl_b` are 128-byte encoded TMA
@@ -141,16 +180,18 @@ struct DescKey {
 };
 // Per-workspace host state of the calls that share it (in stream order).
 struct WorkspaceState {
-    uint32_t epoch = 0;            // last partial-tile epoch handed out
-    uint32_t desc_count = 0;       // expected descriptor counter before the next call
     std::vector<DescKey> descs;    // [group][A, B]: what each descriptor slot holds (empty: unknown)
 };
 // Set up the current device on first use and launch a checked call whose
 // scratch is the workspace at ws_base. With partial_slots > 0 the call may use
 // a split schedule.
 int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles, int block_n, void *ws_base,
-                        int capacity, int prefix_slots, int partial_slots, WorkspaceState *state,
+                        int capacity, int prefix_slots, int partial_slots, int regions, WorkspaceState *state,
                         cudaStream_t stream);
+// Launch a device-table call on the workspace (every group's descriptors are
+// patched by the kernel, in descriptor region 1).
+int launch_device_table(int group_count, const DeviceTable &dt, int block_n, void *ws_base, int capacity,
+                        int slots, WorkspaceState *state, cudaStream_t stream);
 
 // Packer launcher (pack_scales.cu).
 cudaError_t launch_pack_scales(const uint8_t *src, int rows, int k, uint8_t *dst, cudaStream_t stream);

@@ -79,7 +79,7 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int group_count, const nvfp4_problem_s
     e = cudaMemsetAsync(ws, 0, 128, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "clearing the static workspace header");
-    WorkspaceState state;  // counter starts from the cleared header
-    return launch_on_workspace(group_count, args, total, block_n, ws, NVFP4_NOALLOC_MAX_GROUPS, 0, 0, &state,
+    WorkspaceState state;  // empty slot cache: every descriptor is patched
+    return launch_on_workspace(group_count, args, total, block_n, ws, NVFP4_NOALLOC_MAX_GROUPS, 0, 0, 1, &state,
                                reinterpret_cast<cudaStream_t>(stream));
 }

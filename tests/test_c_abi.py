@@ -69,6 +69,22 @@ def test_argument_errors_are_reported_on_the_host(L):
     assert _call([(4, 64, 0, 1)], C={0: 0}) == -1
 
 
+def test_device_table_host_argument_errors(L):
+    """nvfp4_grouped_gemm_device checks what the host can see (count range,
+    null or misaligned arrays) before it touches the GPU; the group rules are
+    checked by the kernel."""
+    vp = ctypes.c_void_p
+    arrays = [vp(0x10000 + 0x100 * i) for i in range(5)]
+    f = L.nvfp4_grouped_gemm_device
+    assert f(0, None, None, None, None, None, None, None) == 0                 # no groups: no-op
+    assert f(-1, vp(0x20000), *arrays, None) == -1
+    assert f(nv.MAX_GROUPS + 1, vp(0x20000), *arrays, None) == -1
+    assert f(2, None, *arrays, None) == -1                                     # null sizes
+    assert f(2, vp(0x20000), None, *arrays[1:], None) == -1                    # null pointer array
+    assert f(2, vp(0x20008), *arrays, None) == -3                              # sizes not 16-byte aligned
+    assert f(2, vp(0x20000), vp(0x10004), *arrays[1:], None) == -3             # pointer array not 8-byte aligned
+
+
 def test_pack_scales_argument_errors(L):
     vp = ctypes.c_void_p
     assert L.nvfp4_pack_scales(vp(0x10000), -1, 64, vp(0x20000), None) == -1
