@@ -246,3 +246,85 @@ void nvfp4_oracle_pack_scales(const uint8_t *sf_rowmajor, int rows, int k, uint8
             sf_atoms[nvfp4_oracle_scale_atom_offset(r, kb, k)] =
                 sf_rowmajor[(size_t)r * (size_t)kbs + (size_t)kb];
 }
+
+/* ---- NVFP4 quantisation of activations ---------------------------------- */
+/*
+ * The quantiser that turns real-valued operands into the NVFP4 pair (e2m1
+ * codes, one e4m3fn scale per 16 K-elements). The submissions receive their
+ * operands already in this form; the quantisation itself is the one the
+ * grouped-GEMM task states for its inputs: per row and 16-element K block,
+ *     amax  = max |x|
+ *     sf    = e4m3fn(amax / 6), round to nearest, ties to the even code,
+ *             saturating at 448
+ *     code  = e2m1(x / dec(sf)), round to nearest, ties to the even code,
+ *             saturating at 6, the sign of x kept (a negative x that rounds
+ *             to zero gives -0, code 8)
+ *     every code is +0 when dec(sf) == 0.
+ * Both quotients are taken in double precision here. For inputs that are
+ * bf16 or fp16 values this decides the same codes as the quotients rounded
+ * to fp32 (neither quotient can land within an fp32 rounding of a rounding
+ * boundary without being on it); the pin tests check that claim exhaustively
+ * over bf16 and fp16.
+ */
+
+/* e4m3fn code nearest to s >= 0 (ties to the even code), 0x7E (448) for
+ * s >= 448. */
+uint32_t nvfp4_oracle_e4m3fn_round(double s)
+{
+    if (!(s < 448.0))
+        return 0x7Eu;
+    uint32_t best = 0;
+    double best_d = INFINITY;
+    for (uint32_t c = 0; c <= 0x7Eu; ++c) {
+        double d = fabs(nvfp4_oracle_e4m3fn_value(c) - s);
+        if (d < best_d || (d == best_d && (c & 1u) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return best;
+}
+
+/* e2m1 code nearest to q (ties to the even code), magnitude saturating at 6,
+ * sign bit from q. */
+uint32_t nvfp4_oracle_e2m1_round(double q)
+{
+    uint32_t sign = signbit(q) ? 8u : 0u;
+    double a = fabs(q);
+    if (a >= 6.0)
+        return sign | 7u;
+    uint32_t best = 0;
+    double best_d = INFINITY;
+    for (uint32_t c = 0; c <= 7u; ++c) {
+        double d = fabs(nvfp4_oracle_e2m1_value(c) - a);
+        if (d < best_d || (d == best_d && (c & 1u) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return sign | best;
+}
+
+/* Quantise x [rows][k] (k % 16 == 0) into codes [rows][k/2] (low nibble = even
+ * k) and row-major scales sf [rows][k/16]. */
+void nvfp4_oracle_quantize(const float *x, int rows, int k, uint8_t *codes, uint8_t *sf)
+{
+    int kbs = k / 16;
+    for (int r = 0; r < rows; ++r) {
+        const float *xr = x + (size_t)r * (size_t)k;
+        uint8_t *cr = codes + (size_t)r * (size_t)(k / 2);
+        for (int b = 0; b < kbs; ++b) {
+            double amax = 0.0;
+            for (int j = 0; j < 16; ++j)
+                amax = fmax(amax, fabs((double)xr[16 * b + j]));
+            uint32_t s = nvfp4_oracle_e4m3fn_round(amax / 6.0);
+            double dec = nvfp4_oracle_e4m3fn_value(s);
+            sf[(size_t)r * (size_t)kbs + (size_t)b] = (uint8_t)s;
+            for (int j = 0; j < 16; j += 2) {
+                uint32_t lo = dec == 0.0 ? 0u : nvfp4_oracle_e2m1_round((double)xr[16 * b + j] / dec);
+                uint32_t hi = dec == 0.0 ? 0u : nvfp4_oracle_e2m1_round((double)xr[16 * b + j + 1] / dec);
+                cr[8 * b + j / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    }
+}

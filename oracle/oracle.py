@@ -76,6 +76,13 @@ def _load():
         lib.nvfp4_oracle_scale_atom_offset.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
         lib.nvfp4_oracle_pack_scales.restype = None
         lib.nvfp4_oracle_pack_scales.argtypes = [u8p, ctypes.c_int, ctypes.c_int, u8p]
+        lib.nvfp4_oracle_e4m3fn_round.restype = ctypes.c_uint32
+        lib.nvfp4_oracle_e4m3fn_round.argtypes = [ctypes.c_double]
+        lib.nvfp4_oracle_e2m1_round.restype = ctypes.c_uint32
+        lib.nvfp4_oracle_e2m1_round.argtypes = [ctypes.c_double]
+        lib.nvfp4_oracle_quantize.restype = None
+        lib.nvfp4_oracle_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_void_p]
         _lib = lib
         return lib
 
@@ -190,3 +197,27 @@ def pack_scales(sf_rowmajor: np.ndarray, k: int) -> np.ndarray:
     _load().nvfp4_oracle_pack_scales(sf.ctypes.data_as(u8p), int(rows), int(k),
                                      out.ctypes.data_as(u8p))
     return out
+
+
+def e4m3fn_round(s: float) -> int:
+    """e4m3fn code nearest to s >= 0, ties to the even code, 448 for s >= 448."""
+    return int(_load().nvfp4_oracle_e4m3fn_round(float(s)))
+
+
+def e2m1_round(q: float) -> int:
+    """e2m1 code nearest to q, ties to the even code, |q| saturating at 6, sign kept."""
+    return int(_load().nvfp4_oracle_e2m1_round(float(q)))
+
+
+def quantize(x: np.ndarray):
+    """NVFP4 quantisation of a real matrix [rows, k] (k % 16 == 0; the values
+    are taken as float32): returns (codes uint8 [rows, k/2], row-major scales
+    uint8 [rows, k/16])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, k = x.shape
+    assert k % 16 == 0
+    codes = np.zeros((rows, k // 2), np.uint8)
+    sf = np.zeros((rows, k // 16), np.uint8)
+    if rows and k:
+        _load().nvfp4_oracle_quantize(x.ctypes.data, rows, k, _ptr(codes), _ptr(sf))
+    return codes, sf
