@@ -1,12 +1,14 @@
 #!/usr/bin/env python3
 """Benchmark of the NVFP4 block-scaled grouped GEMM on GB300.
 
-One step = one grouped call (prologue + persistent GEMM kernel) over the
+One step = one grouped call (one persistent GEMM kernel) over the
 workload's seeded synthetic inputs, resident in HBM, L2 flushed between timed
 calls. Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+  python bench.py --api device ...        # the device-resident group-table entry point
+  python bench.py --op quantize ...       # quantise-and-pack of the workload's activations
 
 N > 1 runs N independent replicas (one process per GPU under torchrun; the
 path has no exchange step); value = all ranks' FLOPs / the slowest rank's time.
@@ -48,6 +50,12 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="decode", choices=list(WORKLOAD_TEXT))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--tile-n", type=int, default=0, help="GEMM tile N (0 = library default)")
+    ap.add_argument("--api", choices=["host", "device"], default="host",
+                    help="host: nvfp4_grouped_gemm (group table from the host); device: "
+                         "nvfp4_grouped_gemm_device (group table in device memory)")
+    ap.add_argument("--op", choices=["gemm", "quantize"], default="gemm",
+                    help="gemm: the grouped GEMM (default); quantize: nvfp4_quantize_pack of the workload's "
+                         "activations (all groups' rows stacked, bf16 [sum m, k])")
     ap.add_argument("--flush-mb", type=int, default=512, help="L2 flush buffer read between timed calls")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -268,11 +276,18 @@ def gpu_arm(args, rank, world, local_rank):
     dp = DeviceProblem.upload(prob, device=dev)   # uploads, then packs scales with the library kernel
     t_pack1.record(stream)
     torch.cuda.synchronize()
+    if args.api == "device":
+        table = nv.DeviceGroupTable(len(dp.problem_sizes), device=dev)
+        table.set(dp.problem_sizes, dp.A, dp.B, dp.SFA, dp.SFB, dp.C)
+        torch.cuda.synchronize()
+        call = lambda: table.run(stream)
+    else:
+        call = lambda: dp.run(stream)
 
     # L2 flush: read a buffer 4x the 129 MB L2 (reads leave no dirty lines to write back)
     flush = torch.ones(args.flush_mb << 18, dtype=torch.int32, device=dev)
     for _ in range(max(3, args.warmup)):
-        dp.run(stream)
+        call()
     torch.cuda.synchronize()
     assert nv.device_status(stream) == 0, "a bounded wait gave up during warm-up"
 
@@ -291,7 +306,7 @@ def gpu_arm(args, rank, world, local_rank):
         for i in range(args.steps):
             flush.sum()                      # evict A/B/scales from L2 (outside the timed events)
             ev[i][0].record(stream)
-            dp.run(stream)
+            call()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -325,7 +340,7 @@ def gpu_arm(args, rank, world, local_rank):
         for _ in range(2):
             for h, d in zip(host_in, dev_in):
                 d.copy_(h, non_blocking=True)
-            dp.run(stream)
+            call()
             for h, c in zip(host_out, dp.C):
                 h.copy_(c, non_blocking=True)
         torch.cuda.synchronize()
@@ -336,7 +351,7 @@ def gpu_arm(args, rank, world, local_rank):
             a.record(stream)
             for h, d in zip(host_in, dev_in):
                 d.copy_(h, non_blocking=True)
-            dp.run(stream)
+            call()
             for h, c in zip(host_out, dp.C):
                 h.copy_(c, non_blocking=True)
             b.record(stream)
@@ -382,7 +397,7 @@ def gpu_arm(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "nvfp4 (e2m1 x e2m1, e4m3 per-16 scales) -> f32 acc -> f16",
         "data": "synthetic (seeded N(0,1) -> NVFP4 per-16 quantisation)",
-        "config": dict(workload_config(args, prob), tile_n=tile_n, parallelism=f"replicas x{world}"),
+        "config": dict(workload_config(args, prob), tile_n=tile_n, api=args.api, parallelism=f"replicas x{world}"),
         "flops_per_call": flops, "bytes_per_call": nbytes,
         "roofline": roof,
         "cpu_baseline": cpu,
@@ -391,6 +406,109 @@ def gpu_arm(args, rank, world, local_rank):
         "scale_pack_us": 1e3 * t_pack0.elapsed_time(t_pack1),
         "clocks": clocks.summary(),
         "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ quantise-and-pack
+
+def quantize_arm(args, rank, world, local_rank):
+    """nvfp4_quantize_pack of the workload's stacked activations (bf16
+    [sum m, k], seeded N(0, 1)); HBM-bound: bytes = 2 rows k in + rows k / 2
+    codes + rows k / 16 scales."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import nvfp4_block_scaled_grouped_gb300 as nv
+    from nvfp4_block_scaled_grouped_gb300 import workloads
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    sizes = workloads.problem_sizes(args.workload, args.seed)
+    rows, k = int(sum(s[0] for s in sizes)), int(max(s[2] for s in sizes))
+    gen = torch.Generator().manual_seed(args.seed)
+    x = torch.randn(rows, k, generator=gen).to(torch.bfloat16).to(dev)
+    codes = torch.empty((rows, k // 2), dtype=torch.uint8, device=dev)
+    sf = torch.empty(nv.scale_bytes(rows, k), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    call = lambda: nv.quantize_pack(x.data_ptr(), nv.DTYPE_BF16, rows, k, codes.data_ptr(), sf.data_ptr(), stream)
+    nbytes = 2 * rows * k + rows * k // 2 + rows * k // 16
+    flush = torch.ones(args.flush_mb << 18, dtype=torch.int32, device=dev)
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(gpu_uuid(local_rank)) as clocks:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(2_000_000)
+        for i in range(args.steps):
+            flush.sum()
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    times_ms = [a.elapsed_time(b) for a, b in ev]
+    t_ms = statistics.fmean(times_ms)
+    if world > 1:
+        t = torch.tensor([t_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_ms = float(t.item())
+    # e2e: bf16 input from pinned host memory, codes and scales back
+    hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    hx.copy_(x)
+    hc = torch.empty(codes.shape, dtype=codes.dtype, pin_memory=True)
+    hs = torch.empty(sf.shape, dtype=sf.dtype, pin_memory=True)
+    e_ms = []
+    for i in range(max(3, min(args.steps, 10)) + 1):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.sum()
+        a.record(stream)
+        x.copy_(hx, non_blocking=True)
+        call()
+        hc.copy_(codes, non_blocking=True)
+        hs.copy_(sf, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i:
+            e_ms.append(a.elapsed_time(b))
+    if rank != 0:
+        return 0
+    peaks, peak_src = measured_peaks()
+    t_s = t_ms * 1e-3
+    roof = {"bound": "hbm", "achieved": nbytes / t_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
+    roof["kernel"] = "quantize_pack_kernel (the only kernel of the call)"
+    cpu = None
+    if not args.no_cpu_baseline:
+        from oracle import oracle
+        xs = x[: max(1, min(rows, 64))].float().cpu().numpy()
+        w0 = time.perf_counter()
+        oracle.quantize(xs)
+        w = time.perf_counter() - w0
+        cpu = {"value": xs.size * 2 / w / 1e9, "unit": "GB/s of bf16 input", "cores": 1, "kind": "oracle",
+               "sample": f"{xs.shape[0]} of {rows} rows", "wall_s": w}
+    em = statistics.fmean(e_ms)
+    line = {
+        "metric": "µs per quantise-and-pack call (bf16 activations -> NVFP4 codes + atom-layout scales)",
+        "value": nbytes / t_s / 1e9, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_ms, "us_per_call": t_ms * 1e3,
+        "us_per_call_p10_p50_p90": [float(v * 1e3) for v in _pcts(times_ms)],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 -> e2m1 + e4m3",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": f"activations of {args.workload}: bf16 [{rows}, {k}]", "rows": rows, "k": k,
+                   "l2": f"flushed between timed calls ({args.flush_mb} MB read)", "parallelism": f"replicas x{world}"},
+        "bytes_per_call": nbytes, "roofline": roof, "cpu_baseline": cpu,
+        "e2e": {"value": nbytes / (em * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": em,
+                "h2d_bytes_per_step": hx.numel() * 2, "d2h_bytes_per_step": hc.numel() + hs.numel()},
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -415,6 +533,8 @@ def main(argv=None):
         torch.cuda.set_device(local_rank)
         dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local_rank))
     try:
+        if args.op == "quantize":
+            return quantize_arm(args, rank, world, local_rank)
         return gpu_arm(args, rank, world, local_rank)
     finally:
         if world > 1:

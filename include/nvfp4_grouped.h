@@ -183,6 +183,35 @@ size_t nvfp4_scale_bytes(int rows, int k);
 int nvfp4_pack_scales(const void *sf_rowmajor, int rows, int k, void *sf_atoms,
                       nvfp4_stream_t stream);
 
+/* Element types of nvfp4_quantize_pack's input. */
+#define NVFP4_DTYPE_BF16 0
+#define NVFP4_DTYPE_F16 1
+
+/*
+ * nvfp4_quantize_pack -- quantise an activation matrix to NVFP4 and write it in
+ * the layouts nvfp4_grouped_gemm reads, in one pass over the input.
+ *   x         DEVICE, [rows][k] bf16 (x_dtype NVFP4_DTYPE_BF16) or fp16
+ *             (NVFP4_DTYPE_F16), row-major, row stride k elements.
+ *   codes     DEVICE, [rows][k/2] bytes: e2m1 codes, two per byte, the even k
+ *             in the low nibble (the A / B layout of nvfp4_grouped_gemm).
+ *   sf_atoms  DEVICE, nvfp4_scale_bytes(rows, k) bytes: e4m3fn scales in the
+ *             atom layout (every byte written, padding 0x00).
+ * Per row and 16-element block: amax = max|x|; sf = e4m3fn(amax / 6), rounded
+ * to nearest (ties to the even code) and saturating at 448; code =
+ * e2m1(x / dec(sf)), rounded to nearest (ties to the even code), saturating
+ * at 6, keeping the sign of x (a negative x that rounds to zero gives -0);
+ * every code is +0 when dec(sf) == 0. This is the quantisation the
+ * "nvfp4 group gemm" task states for its inputs; the submissions receive
+ * their operands already in this form (submission 499344, custom_kernel
+ * docstring). Inputs must be finite (codes for NaN or infinity are
+ * unspecified).
+ * Requires rows >= 0, k >= 0, k % 16 == 0, rows <= 65535 * 128 and 16-byte
+ * aligned pointers; rows == 0 or k == 0 is a no-op. Errors are detected on the
+ * host. The outputs must not overlap x.
+ */
+int nvfp4_quantize_pack(const void *x, int x_dtype, int rows, int k, void *codes, void *sf_atoms,
+                        nvfp4_stream_t stream);
+
 /*
  * nvfp4_device_status -- read and clear the device-side status word of the
  * (current device, stream) workspace. Synchronises `stream`. *status receives

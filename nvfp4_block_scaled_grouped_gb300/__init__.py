@@ -12,6 +12,8 @@ The functions mirror the C entry points:
 * :func:`grouped_gemm_device` / :class:`DeviceGroupTable` --
   ``nvfp4_grouped_gemm_device`` (group table in device memory);
 * :func:`pack_scales` / :func:`scale_bytes` -- the scale-layout packer;
+* :func:`quantize_pack` / :func:`quantize_pack_tensor` -- ``nvfp4_quantize_pack``
+  (bf16 / fp16 activations to e2m1 codes and atom-layout scales);
 * :func:`device_status`, :func:`set_tile_n`.
 """
 from __future__ import annotations
@@ -22,7 +24,7 @@ from pathlib import Path
 
 __all__ = [
     "Nvfp4Error", "lib", "library_path", "grouped_gemm", "grouped_gemm_tensors", "grouped_gemm_device",
-    "DeviceGroupTable", "pack_scales",
+    "DeviceGroupTable", "quantize_pack", "quantize_pack_tensor", "DTYPE_BF16", "DTYPE_F16", "pack_scales",
     "pack_scales_tensor", "scale_bytes", "device_status", "set_tile_n", "MAX_GROUPS", "STATUS",
 ]
 
@@ -66,6 +68,8 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_grouped_gemm.argtypes = [ctypes.c_int, ctypes.POINTER(ProblemSize), vpp, vpp, vpp, vpp, vpp, vp]
         L.nvfp4_grouped_gemm_device.restype = ctypes.c_int
         L.nvfp4_grouped_gemm_device.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, vp, vp]
+        L.nvfp4_quantize_pack.restype = ctypes.c_int
+        L.nvfp4_quantize_pack.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp]
         L.nvfp4_scale_bytes.restype = ctypes.c_size_t
         L.nvfp4_scale_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
         L.nvfp4_pack_scales.restype = ctypes.c_int
@@ -171,6 +175,35 @@ class DeviceGroupTable:
         row = lambda i: self.ptrs[i].data_ptr()
         return grouped_gemm_device(self.group_count, self.sizes.data_ptr(), row(0), row(1), row(2), row(3), row(4),
                                    stream, check=check)
+
+
+DTYPE_BF16, DTYPE_F16 = 0, 1
+
+
+def quantize_pack(x_ptr: int, x_dtype: int, rows: int, k: int, codes_ptr: int, sf_atoms_ptr: int, stream=None,
+                  *, check: bool = True) -> int:
+    """nvfp4_quantize_pack with raw device addresses."""
+    vp = ctypes.c_void_p
+    status = lib().nvfp4_quantize_pack(vp(int(x_ptr) or None), int(x_dtype), int(rows), int(k),
+                                       vp(int(codes_ptr) or None), vp(int(sf_atoms_ptr) or None),
+                                       vp(_stream_handle(stream) or None))
+    if check:
+        _check(status)
+    return status
+
+
+def quantize_pack_tensor(x, stream=None):
+    """torch bf16 / fp16 CUDA tensor [rows, k] -> (codes uint8 [rows, k/2],
+    atom-layout scales uint8 [scale_bytes(rows, k)]), both new tensors."""
+    import torch
+    assert x.dim() == 2 and x.is_contiguous() and x.dtype in (torch.bfloat16, torch.float16)
+    rows, k = x.shape
+    codes = torch.empty((rows, k // 2), dtype=torch.uint8, device=x.device)
+    sf = torch.empty(scale_bytes(rows, k), dtype=torch.uint8, device=x.device)
+    if rows and k:
+        quantize_pack(x.data_ptr(), DTYPE_BF16 if x.dtype == torch.bfloat16 else DTYPE_F16, rows, k,
+                      codes.data_ptr(), sf.data_ptr(), stream)
+    return codes, sf
 
 
 def scale_bytes(rows: int, k: int) -> int:

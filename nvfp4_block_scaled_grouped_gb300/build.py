@@ -19,7 +19,7 @@ CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 BUILD = PKG / "_build"
 LIB = PKG / "_lib" / "libnvfp4_grouped.so"
-SOURCES = ["gemm.cu", "pack_scales.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["gemm.cu", "pack_scales.cu", "quantize.cu", "api.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -476,6 +476,29 @@ int nvfp4_pack_scales(const void *sf_rowmajor, int rows, int k, void *sf_atoms, 
     return NVFP4_OK;
 }
 
+int nvfp4_quantize_pack(const void *x, int x_dtype, int rows, int k, void *codes, void *sf_atoms,
+                        nvfp4_stream_t stream) {
+    if (rows < 0 || k < 0)
+        return fail(NVFP4_ERR_INVALID_ARG, "negative rows (%d) or k (%d)", rows, k);
+    if (x_dtype != NVFP4_DTYPE_BF16 && x_dtype != NVFP4_DTYPE_F16)
+        return fail(NVFP4_ERR_INVALID_ARG, "x_dtype %d is neither NVFP4_DTYPE_BF16 nor NVFP4_DTYPE_F16", x_dtype);
+    if (k % 16 != 0)
+        return fail(NVFP4_ERR_UNSUPPORTED, "k = %d is not a multiple of 16", k);
+    if (rows > 65535 * 128)
+        return fail(NVFP4_ERR_UNSUPPORTED, "rows = %d exceeds %d", rows, 65535 * 128);
+    if (rows == 0 || k == 0)
+        return NVFP4_OK;
+    if (!x || !codes || !sf_atoms)
+        return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(sf_atoms))
+        return fail(NVFP4_ERR_MISALIGNED, "x, codes and sf_atoms must be 16-byte aligned");
+    cudaError_t e = launch_quantize_pack(x, x_dtype == NVFP4_DTYPE_BF16, rows, k, codes, sf_atoms,
+                                         reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "quantise-and-pack launch");
+    return NVFP4_OK;
+}
+
 int nvfp4_device_status(nvfp4_stream_t stream, int *status) {
     if (!status)
         return fail(NVFP4_ERR_INVALID_ARG, "null status");

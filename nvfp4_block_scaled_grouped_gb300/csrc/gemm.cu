@@ -490,6 +490,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_area + 192);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 196);
     volatile int *s_epi_ok = reinterpret_cast<volatile int *>(bar_area + 208);  // [3]: by segment parity, tail
+    volatile uint32_t *s_epoch = reinterpret_cast<volatile uint32_t *>(bar_area + 224);  // this call's epoch
     TailState *s_tail = reinterpret_cast<TailState *>(bar_area + 256);
     static_assert(256 + sizeof(TailState) <= C::kBarrierBytes, "barrier area");
     uint8_t *epi_stage = bar_area + C::kBarrierBytes;                // [4 warps][32 rows][64 B]
@@ -660,8 +661,17 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
             int prev_g = -1;
-            bool descs_ready = !publish;
-            bool ok = true;
+            const uint32_t epoch = call_epoch();
+            *s_epoch = epoch;
+            // every group's descriptors are patched by some CTA at start-up
+            bool ok = !publish || wait_counter(p.ws.desc_count, gridDim.x, abort_flag, p.timeout_ns, p.ws.status);
+            // Once every CTA is past its descriptor wait and has read the
+            // epoch, the last one resets the call counters for the next call.
+            if (atomicAdd(p.ws.done, 1u) == gridDim.x - 1) {
+                *p.ws.desc_count = 0;
+                *p.ws.done = 0;
+                *p.ws.epoch = epoch;
+            }
             Cursor<BN, CAP, DEV> cur = cursor0;
             Segment sg;
             bool any = false;
@@ -675,14 +685,6 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 const int k_blocks = gi.k_blocks;
                 const uint8_t *tmap_a = p.ws.tmaps + (size_t)sg.g * 256;
                 const uint8_t *tmap_b = tmap_a + 128;
-                if (!descs_ready) {
-                    // every group's descriptors are patched by some CTA at start-up
-                    if (!wait_counter(p.ws.desc_count, gridDim.x, abort_flag, p.timeout_ns, p.ws.status)) {
-                        ok = false;
-                        break;
-                    }
-                    descs_ready = true;
-                }
                 if (sg.g != prev_g) {
                     ptx::tmap_acquire(tmap_a);
                     ptx::tmap_acquire(tmap_b);
@@ -725,7 +727,6 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 // tile is copied into the ring, each stage as soon as the MMAs
                 // reading it have completed, oldest stage first.
                 const int cta = blockIdx.x;
-                const uint32_t epoch = call_epoch();
                 int pieces = 0;
                 while (cta + pieces + 1 < P && split_begin(cta + pieces + 1, P, total_work) < sg.w_tile_end)
                     ++pieces;
@@ -931,7 +932,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 ptx::named_barrier(1, 128);
                 if (threadIdx.x == 0) {
                     __threadfence();
-                    ptx::st_release_gpu(p.ws.flags + cta, call_epoch());
+                    ptx::st_release_gpu(p.ws.flags + cta, *s_epoch);
                 }
             }
             if (++acc == C::kAccStages) {
@@ -999,7 +1000,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 ptx::named_barrier(1, 256);
                 if (threadIdx.x == 0) {
                     __threadfence();
-                    ptx::st_release_gpu(p.ws.flags + blockIdx.x, call_epoch());
+                    ptx::st_release_gpu(p.ws.flags + blockIdx.x, *s_epoch);
                 }
             }
         }
@@ -1011,13 +1012,6 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     if (warp == 5) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, C::kTmemCols);
-    }
-    // The last CTA to finish (every other one is past its descriptor wait and
-    // its flag traffic) resets the call counters and records the epoch.
-    if (threadIdx.x == 0 && atomicAdd(p.ws.done, 1u) == gridDim.x - 1) {
-        *p.ws.desc_count = 0;
-        *p.ws.done = 0;
-        *p.ws.epoch = call_epoch();
     }
 }
 

@@ -59,10 +59,11 @@ __host__ __device__ constexpr size_t cta_prefix_bytes(int capacity) { return 2 *
 //               of rejected device-table groups) at byte 0; at byte 64 the
 //               descriptor-publication counter (CTAs that have published their
 //               patched descriptors in the running call), at 96 the count of
-//               CTAs that have finished the running call, at 100 the epoch of
-//               the last completed call. The last CTA of a call to finish
-//               resets both counters and advances the epoch, so nothing on the
-//               host tracks them (calls replayed from a CUDA graph included).
+//               CTAs whose producer has passed the running call's descriptor
+//               wait and read the epoch, at 100 the epoch of the last call.
+//               The last CTA to get there resets both counters and advances
+//               the epoch, so nothing on the host tracks them (calls replayed
+//               from a CUDA graph included).
 //   tmaps       TMA descriptors [regions][capacity][A, B], 128 B each. Region
 //               0 serves eager host-table calls (its contents are cached on
 //               the host); region 1, where present, serves calls whose
@@ -192,6 +193,10 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
 // patched by the kernel, in descriptor region 1).
 int launch_device_table(int group_count, const DeviceTable &dt, int block_n, void *ws_base, int capacity,
                         int slots, WorkspaceState *state, cudaStream_t stream);
+
+// Quantise-and-pack launcher (quantize.cu).
+cudaError_t launch_quantize_pack(const void *x, bool bf16, int rows, int k, void *codes, void *sf_atoms,
+                                 cudaStream_t stream);
 
 // Packer launcher (pack_scales.cu).
 cudaError_t launch_pack_scales(const uint8_t *src, int rows, int k, uint8_t *dst, cudaStream_t stream);

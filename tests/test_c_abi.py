@@ -85,6 +85,19 @@ def test_device_table_host_argument_errors(L):
     assert f(2, vp(0x20000), vp(0x10004), *arrays[1:], None) == -3             # pointer array not 8-byte aligned
 
 
+def test_quantize_pack_host_argument_errors(L):
+    vp = ctypes.c_void_p
+    f = L.nvfp4_quantize_pack
+    x, c, s = vp(0x10000), vp(0x20000), vp(0x30000)
+    assert f(x, 0, 0, 64, c, s, None) == 0                 # no rows: no-op
+    assert f(x, 1, 4, 0, c, s, None) == 0                  # k == 0: no-op
+    assert f(x, 0, -1, 64, c, s, None) == -1
+    assert f(x, 7, 4, 64, c, s, None) == -1                # unknown input type
+    assert f(x, 0, 4, 40, c, s, None) == -2                # k % 16
+    assert f(None, 0, 4, 64, c, s, None) == -1
+    assert f(vp(0x10008), 1, 4, 64, c, s, None) == -3      # misaligned
+
+
 def test_pack_scales_argument_errors(L):
     vp = ctypes.c_void_p
     assert L.nvfp4_pack_scales(vp(0x10000), -1, 64, vp(0x20000), None) == -1
