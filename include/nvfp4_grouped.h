@@ -39,8 +39,10 @@ extern "C" {
 typedef struct CUstream_st *nvfp4_stream_t;
 
 /* Per-group problem size, as in the submissions' problem_sizes list: (m, n, k, l).
- * l is the batch count of the group and must be 1 for non-empty groups
- * (submission 499344 docstring: l is always 1). */
+ * l is the batch count of the group: l independent products of the same
+ * shape (the submissions' benchmarks use l = 1, submission 499344 docstring;
+ * their operand layouts carry l as the outermost mode, submission 506336,
+ * where the per-group tensors are built). l == 0 makes the group empty. */
 typedef struct nvfp4_problem_size {
     int32_t m, n, k, l;
 } nvfp4_problem_size;
@@ -48,7 +50,7 @@ typedef struct nvfp4_problem_size {
 typedef enum nvfp4_status {
     NVFP4_OK = 0,
     NVFP4_ERR_INVALID_ARG = -1, /* null array, negative size, null pointer in a non-empty group, too many groups */
-    NVFP4_ERR_UNSUPPORTED = -2, /* l != 1, k % 32 != 0 or n % 32 != 0 in a non-empty group, sizes too large */
+    NVFP4_ERR_UNSUPPORTED = -2, /* k % 32 != 0 or n % 32 != 0 in a non-empty group, sizes too large */
     NVFP4_ERR_MISALIGNED = -3,  /* a pointer of a non-empty group is not 16-byte aligned */
     NVFP4_ERR_CUDA = -4,        /* a CUDA runtime/driver call or a launch failed */
     NVFP4_ERR_TIMEOUT = -5      /* a kernel's bounded wait ran out (reported by nvfp4_device_status) */
@@ -61,7 +63,10 @@ typedef enum nvfp4_status {
  * nvfp4_grouped_gemm -- the grouped block-scaled GEMM.
  *
  * problem_sizes, A, B, SFA, SFB, C: HOST arrays of group_count entries. The
- * pointer arrays hold DEVICE addresses:
+ * pointer arrays hold DEVICE addresses (shown for l = 1; a group with l
+ * batches stacks them batch-outermost: A [l][m][k/2], B [l][n][k/2],
+ * C [l][m][n], SFA / SFB l consecutive atom blocks of nvfp4_scale_bytes(m, k)
+ * / nvfp4_scale_bytes(n, k) bytes, batch b computed from batch b alone):
  *   A[g]   e2m1 codes, [m][k/2] bytes, K-major, two codes per byte (the even k
  *          in the low nibble), row stride k/2 bytes.
  *   B[g]   e2m1 codes, [n][k/2] bytes, same layout.
@@ -73,10 +78,11 @@ typedef enum nvfp4_status {
  *          Scales must be non-negative and not NaN.
  *   SFB[g] e4m3fn scales of B, nvfp4_scale_bytes(n, k) bytes, same layout.
  *   C[g]   fp16, [m][n] row-major, written in full; nothing else is written.
- * Group rules: a group with m == 0 or n == 0 is skipped and its pointers are
- * not read (they may be null); a group with k == 0 and m, n > 0 gets C = +0.
- * Non-empty groups need l == 1, k % 32 == 0, n % 32 == 0 and 16-byte aligned
- * pointers (A, B, SFA, SFB may be null when k == 0).
+ * Group rules: a group with m == 0, n == 0 or l == 0 is skipped and its
+ * pointers are not read (they may be null); a group with k == 0 and m, n, l > 0
+ * gets C = +0. Non-empty groups need k % 32 == 0, n % 32 == 0, l <= 65535,
+ * l*m and l*n <= 2^31 - 1 and 16-byte aligned pointers (A, B, SFA, SFB may be
+ * null when k == 0).
  * The library keeps a small device workspace per (device, stream), allocated
  * on the first call for that pair and reused in stream order.
  */
@@ -105,7 +111,8 @@ int nvfp4_grouped_gemm(int group_count, const nvfp4_problem_size *problem_sizes,
  *                    nvfp4_grouped_gemm.
  * The arrays are read by the kernel when it runs (in stream order), not when
  * the call returns; they must stay valid and unchanged until then.
- * Group rules are those of nvfp4_grouped_gemm plus m, n, k <= 2^24; they are
+ * Group rules are those of nvfp4_grouped_gemm plus m, n, k <= 2^24 and
+ * l*m, l*n <= 2^30; they are
  * checked on the device: a group that breaks one is skipped (its C is not
  * written), the rest of the call completes, and the next nvfp4_device_status
  * on the stream reports NVFP4_ERR_INVALID_ARG. Only the host arguments are

@@ -180,11 +180,15 @@ int check_groups(int group_count, int max_groups, const nvfp4_problem_size *prob
         const nvfp4_problem_size &s = problem_sizes[g];
         if (s.m < 0 || s.n < 0 || s.k < 0 || s.l < 0)
             return fail(NVFP4_ERR_INVALID_ARG, "group %d: negative size (%d, %d, %d, %d)", g, s.m, s.n, s.k, s.l);
-        args[g] = GroupArgs{s.m, s.n, s.k, 3, A[g], B[g], SFA[g], SFB[g], C[g]};
-        if (s.m == 0 || s.n == 0)
+        args[g] = GroupArgs{s.m, s.n, s.k, (uint16_t)(s.l <= kMaxBatch ? s.l : 0), 3, A[g], B[g], SFA[g], SFB[g],
+                            C[g]};
+        if (s.m == 0 || s.n == 0 || s.l == 0) {
+            args[g].m = args[g].n = 0;  // empty: nothing is read or written
             continue;
-        if (s.l != 1)
-            return fail(NVFP4_ERR_UNSUPPORTED, "group %d: l = %d (only l = 1 is supported)", g, s.l);
+        }
+        if (s.l > kMaxBatch || (long long)s.l * s.m > 0x7fffffffLL || (long long)s.l * s.n > 0x7fffffffLL)
+            return fail(NVFP4_ERR_UNSUPPORTED, "group %d: l = %d with m = %d, n = %d is too large", g, s.l, s.m,
+                        s.n);
         if (s.k % 32 != 0 || s.n % 32 != 0)
             return fail(NVFP4_ERR_UNSUPPORTED, "group %d: k = %d and n = %d must be multiples of 32", g, s.k, s.n);
         if (!C[g])
@@ -197,7 +201,7 @@ int check_groups(int group_count, int max_groups, const nvfp4_problem_size *prob
             if (!aligned16(A[g]) || !aligned16(B[g]) || !aligned16(SFA[g]) || !aligned16(SFB[g]))
                 return fail(NVFP4_ERR_MISALIGNED, "group %d: A/B/SFA/SFB not 16-byte aligned", g);
         }
-        total += (long long)((s.m + kBlockM - 1) / kBlockM) * (long long)((s.n + block_n - 1) / block_n);
+        total += (long long)((s.m + kBlockM - 1) / kBlockM) * (long long)((s.n + block_n - 1) / block_n) * s.l;
         if (total > 0x7fffffffLL)
             return fail(NVFP4_ERR_UNSUPPORTED, "more than 2^31 - 1 tiles");
     }
@@ -247,7 +251,8 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
         const GroupArgs &a = args[g];
         if (a.m <= 0 || a.n <= 0)
             continue;
-        const long long tiles = (long long)((a.m + kBlockM - 1) / kBlockM) * ((a.n + block_n - 1) / block_n);
+        const long long tiles =
+            (long long)((a.m + kBlockM - 1) / kBlockM) * ((a.n + block_n - 1) / block_n) * (long long)a.l;
         const long long kt = (a.k + kBlockK - 1) / kBlockK;
         total_work += tiles * (kt > 1 ? kt : 1);
     }
@@ -288,7 +293,7 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
             a.patch = 0;
             if (a.m <= 0 || a.n <= 0 || a.k <= 0)
                 continue;
-            const DescKey ka{a.a, a.m, a.k, kBlockM}, kb{a.b, a.n, a.k, block_n};
+            const DescKey ka{a.a, (int32_t)a.l * a.m, a.k, kBlockM}, kb{a.b, (int32_t)a.l * a.n, a.k, block_n};
             if (graph || !(state->descs[2 * g] == ka)) {
                 a.patch |= 1;
                 ++desc_maps;
@@ -320,9 +325,9 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
     for (int g = 0; g < group_count; ++g) {
         const GroupArgs &a = args[g];
         if (a.patch & 1)
-            state->descs[2 * g] = DescKey{a.a, a.m, a.k, kBlockM};
+            state->descs[2 * g] = DescKey{a.a, (int32_t)a.l * a.m, a.k, kBlockM};
         if (a.patch & 2)
-            state->descs[2 * g + 1] = DescKey{a.b, a.n, a.k, block_n};
+            state->descs[2 * g + 1] = DescKey{a.b, (int32_t)a.l * a.n, a.k, block_n};
     }
     return NVFP4_OK;
 }

@@ -116,9 +116,10 @@ struct GemmParams {
 
 __device__ __forceinline__ bool aligned16(const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
 
-// Largest m, n or k of a device-table group (keeps every tile and unit count
-// of a call inside int32).
+// Largest m, n or k, and l*m or l*n, of a device-table group (keeps every
+// tile and unit count of a call inside int32).
 constexpr int kDeviceTableMaxDim = 1 << 24;
+constexpr long long kDeviceTableMaxRows = 1ll << 30;
 
 // Group g's arguments: the kernel parameter's entry, or the caller's device
 // arrays checked against the same rules as the host entry point; a group that
@@ -133,6 +134,7 @@ __device__ __forceinline__ GroupArgs load_group(const GemmParams<CAP, DEV> &p, i
         a.m = sz.x;
         a.n = sz.y;
         a.k = sz.z;
+        a.l = (uint16_t)(sz.w >= 0 && sz.w <= kMaxBatch ? sz.w : 0);
         a.patch = 3;
         a.a = p.dt.a[g];
         a.b = p.dt.b[g];
@@ -140,9 +142,10 @@ __device__ __forceinline__ GroupArgs load_group(const GemmParams<CAP, DEV> &p, i
         a.sfb = p.dt.sfb[g];
         a.c = p.dt.c[g];
         bool ok = a.m >= 0 && a.n >= 0 && a.k >= 0 && sz.w >= 0 && a.m <= kDeviceTableMaxDim &&
-                  a.n <= kDeviceTableMaxDim && a.k <= kDeviceTableMaxDim;
-        if (ok && a.m > 0 && a.n > 0) {
-            ok = sz.w == 1 && a.k % 32 == 0 && a.n % 32 == 0 && a.c && aligned16(a.c);
+                  a.n <= kDeviceTableMaxDim && a.k <= kDeviceTableMaxDim && sz.w <= kMaxBatch;
+        if (ok && a.m > 0 && a.n > 0 && sz.w > 0) {
+            ok = (long long)sz.w * a.m <= kDeviceTableMaxRows && (long long)sz.w * a.n <= kDeviceTableMaxRows &&
+                 a.k % 32 == 0 && a.n % 32 == 0 && a.c && aligned16(a.c);
             if (ok && a.k > 0)
                 ok = a.a && a.b && a.sfa && a.sfb && aligned16(a.a) && aligned16(a.b) && aligned16(a.sfa) &&
                      aligned16(a.sfb);
@@ -160,11 +163,13 @@ __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b
 
 // Derived sizes of one group (m, n, k >= 0).
 struct GInfo {
-    int m, n, k;
-    int tiles_m, tiles;       // ceil(m / 128), ceil(m / 128) * ceil(n / BN) (0 for an empty group)
+    int m, n, k, l;
+    int tiles_m, tiles_mn;    // ceil(m / 128), ceil(m / 128) * ceil(n / BN) (0 for an empty group)
+    int tiles;                // tiles_mn * l
     int k_tiles, k_blocks;    // ceil(k / 256), ceil(k / 64)
     int work_tiles;           // max(k_tiles, 1): schedule units per output tile
     int sf_row_blocks_b;      // ceil(n / 128): 128-row scale blocks of B
+    size_t sfa_batch, sfb_batch;  // bytes of one batch's scale atoms
     const uint8_t *sfa, *sfb;
     void *c;
 };
@@ -175,12 +180,16 @@ __device__ __forceinline__ GInfo group_info(const GroupArgs &a) {
     g.m = a.m;
     g.n = a.n;
     g.k = a.k;
+    g.l = a.l;
     g.tiles_m = ceil_div_i(a.m, kBlockM);
-    g.tiles = (a.m > 0 && a.n > 0) ? g.tiles_m * ceil_div_i(a.n, BN) : 0;
+    g.tiles_mn = (a.m > 0 && a.n > 0) ? g.tiles_m * ceil_div_i(a.n, BN) : 0;
+    g.tiles = g.tiles_mn * (int)a.l;
     g.k_tiles = ceil_div_i(a.k, kBlockK);
     g.k_blocks = ceil_div_i(a.k, kMmaK);
     g.work_tiles = g.k_tiles > 1 ? g.k_tiles : 1;
     g.sf_row_blocks_b = ceil_div_i(a.n, 128);
+    g.sfa_batch = (size_t)g.tiles_m * g.k_blocks * kSfAtomBytes;
+    g.sfb_batch = (size_t)g.sf_row_blocks_b * g.k_blocks * kSfAtomBytes;
     g.sfa = static_cast<const uint8_t *>(a.sfa);
     g.sfb = static_cast<const uint8_t *>(a.sfb);
     g.c = a.c;
@@ -240,7 +249,7 @@ __device__ __forceinline__ bool wait_counter(const uint32_t *counter, uint32_t t
 // A run of one tile's k-tiles [kt0, kt1) (out of ktg schedule units) that one
 // CTA processes.
 struct Segment {
-    int g, tm, tn;
+    int g, b, tm, tn;  // group, batch, m-tile, n-tile
     int kt0, kt1, ktg;
     int w_tile_end;  // schedule index one past the tile's last unit
 };
@@ -280,8 +289,10 @@ struct Cursor {
             s.kt0 = local - t * gi.work_tiles;
             const int rest = w_end - w;
             s.kt1 = s.kt0 + ((s.ktg - s.kt0) < rest ? (s.ktg - s.kt0) : rest);
-            s.tm = t % gi.tiles_m;
-            s.tn = t / gi.tiles_m;
+            s.b = t / gi.tiles_mn;
+            const int tb = t - s.b * gi.tiles_mn;
+            s.tm = tb % gi.tiles_m;
+            s.tn = tb / gi.tiles_m;
             w += s.kt1 - s.kt0;
         } else {
             if (tile >= total_tiles)
@@ -289,8 +300,10 @@ struct Cursor {
             s.g = find_group(prefix, group_count, tile);
             const GInfo gi = group_info<BN>(load_group(*prm, s.g));
             t = tile - prefix[s.g];
-            s.tm = t % gi.tiles_m;
-            s.tn = t / gi.tiles_m;
+            s.b = t / gi.tiles_mn;
+            const int tb = t - s.b * gi.tiles_mn;
+            s.tm = tb % gi.tiles_m;
+            s.tn = tb / gi.tiles_m;
             s.ktg = gi.work_tiles;
             s.kt0 = 0;
             s.kt1 = s.ktg;
@@ -344,7 +357,7 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, con
     const int r_local = quarter * 32 + lane;
     const int row = sg.tm * kBlockM + r_local;
     const uint32_t t_row = t_acc + ((uint32_t)(quarter * 32) << 16);
-    __half *c_base = static_cast<__half *>(gi.c);
+    __half *c_base = static_cast<__half *>(gi.c) + (size_t)sg.b * (size_t)m * (size_t)n;
     // fp16 row segment (64 B, 16 words) of chunk cc -> the staging buffer,
     // 16-byte pieces XOR-swizzled by (row / 2) % 4 so that neither the
     // row-wise writes nor the transposed reads conflict on banks; then 4 lanes
@@ -526,7 +539,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         uint32_t patched = 0;
         for (int g = blockIdx.x + lane * gridDim.x; g < group_count; g += 32 * gridDim.x) {
             const GroupArgs a = load_group(p, g);
-            if (a.m <= 0 || a.n <= 0 || a.k <= 0)
+            if (a.m <= 0 || a.n <= 0 || a.k <= 0 || a.l == 0)
                 continue;
             const uint32_t row_bytes = (uint32_t)(a.k / 2);
             for (int which = 0; which < 2; ++which) {
@@ -538,7 +551,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 for (int q = 0; q < 8; ++q)
                     reinterpret_cast<uint4 *>(t)[q] = src[q];
                 ptx::tmap_set_address(t, which ? a.b : a.a);
-                ptx::tmap_set_dims(t, row_bytes, (uint32_t)(which ? a.n : a.m));
+                ptx::tmap_set_dims(t, row_bytes, (uint32_t)a.l * (uint32_t)(which ? a.n : a.m));
                 ptx::tmap_set_stride1(t, row_bytes);
                 ++patched;
             }
@@ -573,7 +586,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 long long t = 0, w = 0;
                 if (g < group_count) {
                     const GroupArgs a = load_group(p, g, &bad);
-                    t = (a.m > 0 && a.n > 0) ? (long long)ceil_div_i(a.m, kBlockM) * ceil_div_i(a.n, BN) : 0;
+                    t = (a.m > 0 && a.n > 0) ? (long long)ceil_div_i(a.m, kBlockM) * ceil_div_i(a.n, BN) * a.l : 0;
                     const int kt = ceil_div_i(a.k, kBlockK);
                     w = t * (kt > 1 ? kt : 1);
                 }
@@ -614,7 +627,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
 #pragma unroll 4
             for (int g = 0; g < group_count; ++g) {
                 const GroupArgs &a = p.groups[g];
-                const int tiles = (a.m > 0 && a.n > 0) ? ceil_div_i(a.m, kBlockM) * ceil_div_i(a.n, BN) : 0;
+                const int tiles = (a.m > 0 && a.n > 0) ? ceil_div_i(a.m, kBlockM) * ceil_div_i(a.n, BN) * a.l : 0;
                 const int kt = ceil_div_i(a.k, kBlockK);
                 if (lane == (g & 31)) {
                     prefix[g] = bt;
@@ -690,10 +703,11 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                     ptx::tmap_acquire(tmap_b);
                     prev_g = sg.g;
                 }
-                const uint8_t *sfa = gi.sfa + (size_t)sg.tm * k_blocks * kSfAtomBytes;
+                const uint8_t *sfa = gi.sfa + (size_t)sg.b * gi.sfa_batch + (size_t)sg.tm * k_blocks * kSfAtomBytes;
                 int sfb_blocks = gi.sf_row_blocks_b - sg.tn * C::kSfbRowBlocks;
                 sfb_blocks = sfb_blocks < C::kSfbRowBlocks ? sfb_blocks : C::kSfbRowBlocks;
-                const uint8_t *sfb = gi.sfb + (size_t)sg.tn * C::kSfbRowBlocks * k_blocks * kSfAtomBytes;
+                const uint8_t *sfb =
+                    gi.sfb + (size_t)sg.b * gi.sfb_batch + (size_t)sg.tn * C::kSfbRowBlocks * k_blocks * kSfAtomBytes;
                 for (int kt = sg.kt0; kt < kend; ++kt) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns, p.ws.status,
                                       kStatusProducerTimeout)) {
@@ -705,8 +719,11 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                     const uint32_t st = smem_base + stage * C::kStageBytes;
                     const uint32_t fb = full_bar(stage);
                     ptx::mbar_arrive_expect_tx(fb, C::kABytes + C::kBBytes + sf_bytes * (1 + sfb_blocks));
-                    ptx::tma_load_2d(st, tmap_a, kt * 128, sg.tm * kBlockM, fb, pol_a);
-                    ptx::tma_load_2d(st + C::kABytes, tmap_b, kt * 128, sg.tn * BN, fb, pol_b);
+                    // batch b's rows start at b * m (b * n) of the group's stack;
+                    // rows a tile reads past its batch only reach accumulator
+                    // rows / columns that the epilogue does not store
+                    ptx::tma_load_2d(st, tmap_a, kt * 128, sg.b * gi.m + sg.tm * kBlockM, fb, pol_a);
+                    ptx::tma_load_2d(st + C::kABytes, tmap_b, kt * 128, sg.b * gi.n + sg.tn * BN, fb, pol_b);
                     ptx::bulk_load(st + C::kABytes + C::kBBytes, sfa + (size_t)(4 * kt) * kSfAtomBytes, sf_bytes,
                                    fb, pol_a);
                     for (int j = 0; j < sfb_blocks; ++j)

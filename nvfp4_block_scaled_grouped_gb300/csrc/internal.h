@@ -21,13 +21,18 @@ constexpr int kMmaK = 64;
 constexpr int kSfAtomBytes = 512;  // 128 rows x 4 scale blocks
 
 // A group's arguments, passed to the GEMM kernel as a kernel parameter.
+// l is the group's batch count: batch b of A starts l-major at row b*m of a
+// [l*m][k/2] stack (likewise B, C and the per-batch scale-atom blocks).
 // `patch` tells the kernel which of the group's descriptors (bit 0: A, bit 1:
 // B) must be rewritten; the others already hold this group's pointer and shape.
 struct GroupArgs {
-    int32_t m, n, k, patch;
+    int32_t m, n, k;
+    uint16_t l, patch;
     const void *a, *b, *sfa, *sfb;
     void *c;
 };
+static_assert(sizeof(GroupArgs) == 56, "kernel parameter budget");
+constexpr int kMaxBatch = 65535;  // largest l
 
 // A call whose group table stays in device memory: the caller's arrays of
 // group_count sizes and pointers, read by the kernel (nothing on the host).

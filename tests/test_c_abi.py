@@ -58,7 +58,10 @@ def test_argument_errors_are_reported_on_the_host(L):
     assert L.nvfp4_grouped_gemm(1, None, None, None, None, None, None, None) == -1
     assert _call([(4, 64, 64, 1)] * (nv.MAX_GROUPS + 1)) == -1             # too many groups
     assert _call([(-1, 64, 64, 1)]) == -1                                  # negative size
-    assert _call([(4, 64, 64, 2)]) == -2                                   # l != 1
+    assert _call([(4, 64, 64, 65536)]) == -2                               # l above 65535
+    assert _call([(40000, 64, 64, 60000)]) == -2                           # l * m above 2^31 - 1
+    assert _call([(4, 64, 64, -1)]) == -1                                  # negative l
+    assert _call([(4, 64, 64, 0), (0, 64, 64, 3)]) == 0                    # l == 0 or m == 0: empty, no-op
     assert _call([(4, 64, 48, 1)]) == -2                                   # k % 32
     assert _call([(4, 48, 64, 1)]) == -2                                   # n % 32
     assert _call([(4, 64, 64, 1)], C={0: 0}) == -1                         # null C

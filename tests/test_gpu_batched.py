@@ -1,0 +1,90 @@
+"""GPU parity of groups with l > 1 batches against the CPU oracle.
+
+A group (m, n, k, l) holds l independent products stacked batch-outermost,
+the layout of the submissions' (m, k, l) operands with strides (k, 1, m*k):
+A [l*m][k/2], B [l*n][k/2], C [l*m][n], and per-batch scale-atom blocks
+(nvfp4_scale_bytes(m, k) bytes each) one after another. Each batch must match
+the oracle's product of that batch alone.
+"""
+import numpy as np
+import pytest
+import torch
+
+from parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    from nvfp4_block_scaled_grouped_gb300 import build
+    build.build_library()
+    import nvfp4_block_scaled_grouped_gb300 as nv
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.init()
+    return nv
+
+
+@pytest.fixture(autouse=True)
+def _reset(nv, monkeypatch):
+    monkeypatch.delenv("NVFP4_SPLIT", raising=False)
+    yield
+    nv.set_tile_n(0)
+
+
+SIZES = [(130, 96, 288, 3), (1, 32, 32, 5), (0, 64, 64, 2), (64, 256, 512, 2), (200, 160, 7168, 2),
+         (77, 64, 0, 2), (40, 64, 256, 0), (129, 384, 1024, 1)]
+
+
+def _batched(nv, sizes, seed):
+    """Per group: the l batch problems (host, row-major scales) and the stacked
+    device buffers."""
+    from nvfp4_block_scaled_grouped_gb300 import workloads
+    groups = []
+    for g, (m, n, k, l) in enumerate(sizes):
+        batches = [workloads.make_problem("tiny", seed=seed * 1000 + 10 * g + b, sizes=[(m, n, k, 1)])
+                   for b in range(l)]
+        dev = lambda arrs: torch.from_numpy(np.ascontiguousarray(np.concatenate(arrs))).cuda() if arrs else None
+        A = dev([p.A[0] for p in batches]) if l else torch.empty(0, dtype=torch.uint8, device="cuda")
+        B = dev([p.B[0] for p in batches]) if l else torch.empty(0, dtype=torch.uint8, device="cuda")
+        pack = lambda sf, rows: (nv.pack_scales_tensor(torch.from_numpy(np.ascontiguousarray(sf)).cuda(), k)
+                                 if rows > 0 and k > 0 else torch.empty(0, dtype=torch.uint8, device="cuda"))
+        SFA = torch.cat([pack(p.SFA[0], m) for p in batches]) if l else torch.empty(0, dtype=torch.uint8,
+                                                                                     device="cuda")
+        SFB = torch.cat([pack(p.SFB[0], n) for p in batches]) if l else torch.empty(0, dtype=torch.uint8,
+                                                                                     device="cuda")
+        C = torch.full((max(l * m, 0), n), 0x7E00, dtype=torch.int16, device="cuda").view(torch.float16)
+        groups.append((batches, A, B, SFA, SFB, C))
+    return groups
+
+
+def _check(oracle_mod, sizes, groups, what):
+    for g, ((m, n, k, l), (batches, _, _, _, _, C)) in enumerate(zip(sizes, groups)):
+        if m == 0 or n == 0 or l == 0:
+            continue
+        c = C.cpu().numpy().reshape(l, m, n)
+        for b, p in enumerate(batches):
+            if k == 0:
+                np.testing.assert_array_equal(c[b].view(np.uint16), np.zeros((m, n), np.uint16))
+                continue
+            ref = oracle_mod.grouped_gemm(p.problem_sizes, p.A, p.B, p.SFA, p.SFB)[0]
+            assert_parity(c[b], ref, f"{what} group {g} batch {b} {(m, n, k, l)}")
+
+
+@pytest.mark.parametrize("api", ["host", "device"])
+@pytest.mark.parametrize("block_n,split", [(128, "0"), (256, "0"), (256, "1"), (128, None)])
+def test_batched_groups(nv, oracle_mod, monkeypatch, api, block_n, split):
+    if split is not None:
+        monkeypatch.setenv("NVFP4_SPLIT", split)
+    nv.set_tile_n(block_n)
+    groups = _batched(nv, SIZES, seed=7)
+    cols = list(zip(*[(A, B, SFA, SFB, C) for (_, A, B, SFA, SFB, C) in groups]))
+    if api == "host":
+        nv.grouped_gemm_tensors(SIZES, *cols)
+    else:
+        t = nv.DeviceGroupTable(len(SIZES))
+        t.set(SIZES, *cols)
+        t.run()
+    torch.cuda.synchronize()
+    assert nv.device_status() == 0
+    _check(oracle_mod, SIZES, groups, f"{api} BN={block_n} split={split}")

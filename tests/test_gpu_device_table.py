@@ -185,10 +185,10 @@ def test_host_table_capture_survives_slot_reuse(nv, oracle_mod):
 
 
 def test_device_table_rejects_bad_groups_on_device(nv, oracle_mod):
-    """Groups that break the rules (l != 1, k % 32 != 0, misaligned C) are
+    """Groups that break the rules (l > 65535, k % 32 != 0, misaligned C) are
     skipped by the kernel -- their C untouched -- while the valid groups are
     computed; the stream's status then reports NVFP4_ERR_INVALID_ARG."""
-    sizes = [(40, 64, 256, 1), (16, 64, 256, 2), (70, 96, 256, 1), (8, 32, 48, 1), (9, 64, 256, 1)]
+    sizes = [(40, 64, 256, 1), (16, 64, 256, 70000), (70, 96, 256, 1), (8, 32, 48, 1), (9, 64, 256, 1)]
     prob = _make([(40, 64, 256, 1), (16, 64, 256, 1), (70, 96, 256, 1), (8, 32, 64, 1), (9, 64, 256, 1)],
                  seed=71)
     dp = _upload(prob)
