@@ -176,6 +176,23 @@ class ClockSampler:
                 "power_w_max": max(pw) if pw else None}
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x; every rank calls it (one rank: x)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(work_per_rank: float, world: int, t_max_s: float) -> float:
+    """Whole-job rate of N independent replicas: all ranks' work over the
+    slowest rank's time."""
+    return world * work_per_rank / t_max_s
+
+
 def gpu_uuid(dev_index):
     import torch
     try:
@@ -334,12 +351,8 @@ def gpu_arm(args, rank, world, local_rank):
     times_ms = [a.elapsed_time(b) for a, b in ev]
     assert nv.device_status(stream) == 0, "a bounded wait gave up during the timed run"
     t_ms = statistics.fmean(times_ms)
-    t_max = t_ms
-    if world > 1:
-        t = torch.tensor([t_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
-    value = world * flops / (t_max * 1e-3) / 1e12
+    t_max = max_over_ranks(t_ms, world, dev)
+    value = replica_throughput(flops, world, t_max * 1e-3) / 1e12
 
     # ---- e2e: host buffers in pinned memory, copies inside the timed region
     e2e = None
@@ -377,12 +390,8 @@ def gpu_arm(args, rank, world, local_rank):
             b.record(stream)
             b.synchronize()
             e_ms.append(a.elapsed_time(b))
-        em = statistics.fmean(e_ms)
-        if world > 1:
-            t = torch.tensor([em], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            em = float(t.item())
-        e2e = {"value": world * flops / (em * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        em = max_over_ranks(statistics.fmean(e_ms), world, dev)
+        e2e = {"value": replica_throughput(flops, world, em * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": em, "steps": e2e_steps}
 
     if rank != 0:
@@ -479,11 +488,7 @@ def quantize_arm(args, rank, world, local_rank):
         if world > 1:
             dist.barrier()
     times_ms = [a.elapsed_time(b) for a, b in ev]
-    t_ms = statistics.fmean(times_ms)
-    if world > 1:
-        t = torch.tensor([t_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_ms = float(t.item())
+    t_ms = max_over_ranks(statistics.fmean(times_ms), world, dev)
     # e2e: bf16 input from pinned host memory, codes and scales back
     hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     hx.copy_(x)
@@ -502,6 +507,7 @@ def quantize_arm(args, rank, world, local_rank):
         b.synchronize()
         if i:
             e_ms.append(a.elapsed_time(b))
+    em = max_over_ranks(statistics.fmean(e_ms), world, dev)   # every rank takes part
     if rank != 0:
         return 0
     peaks, peak_src = measured_peaks()
@@ -520,10 +526,10 @@ def quantize_arm(args, rank, world, local_rank):
         w = time.perf_counter() - w0
         cpu = {"value": xs.size * 2 / w / 1e9, "unit": "GB/s of bf16 input", "cores": 1, "kind": "oracle",
                "sample": f"{xs.shape[0]} of {rows} rows", "wall_s": w}
-    em = statistics.fmean(e_ms)
     line = {
         "metric": "µs per quantise-and-pack call (bf16 activations -> NVFP4 codes + atom-layout scales)",
-        "value": nbytes / t_s / 1e9, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "value": replica_throughput(nbytes, world, t_s) / 1e9, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup,
         "ms_per_step": t_ms, "us_per_call": t_ms * 1e3,
         "us_per_call_p10_p50_p90": [float(v * 1e3) for v in _pcts(times_ms)],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 -> e2m1 + e4m3",
@@ -531,7 +537,7 @@ def quantize_arm(args, rank, world, local_rank):
         "config": {"workload": f"activations of {args.workload}: bf16 [{rows}, {k}]", "rows": rows, "k": k,
                    "l2": f"flushed between timed calls ({args.flush_mb} MB read)", "parallelism": f"replicas x{world}"},
         "bytes_per_call": nbytes, "roofline": roof, "cpu_baseline": cpu,
-        "e2e": {"value": nbytes / (em * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": em,
+        "e2e": {"value": replica_throughput(nbytes, world, em * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": em,
                 "h2d_bytes_per_step": hx.numel() * 2, "d2h_bytes_per_step": hc.numel() + hs.numel()},
         "gpu_launches": args.steps, "clocks": clocks.summary(),
     }

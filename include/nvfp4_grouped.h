@@ -92,6 +92,27 @@ int nvfp4_grouped_gemm(int group_count, const nvfp4_problem_size *problem_sizes,
                        void *const *C, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_grouped_gemm_batched -- several independent grouped problems in one
+ * launch: problem p owns the group_counts[p] consecutive entries that follow
+ * those of problems 0..p-1 in problem_sizes, A, B, SFA, SFB and C (HOST
+ * arrays, layouts as in nvfp4_grouped_gemm). The result of every problem is
+ * the one its own nvfp4_grouped_gemm call would give (within the parity
+ * rule; bit-identical unless a K-split schedule is chosen), and all of them
+ * come from one kernel launch over the sum of the group counts, which must
+ * not exceed NVFP4_MAX_GROUPS. This is the merged launch of submission
+ * 506336 (its host code that concatenates the group tables of one benchmark
+ * call's problems into a single launch), offered as an entry point.
+ * Errors: problem_count < 0, null group_counts, a negative count or a sum
+ * above NVFP4_MAX_GROUPS give NVFP4_ERR_INVALID_ARG; the groups are checked
+ * as in nvfp4_grouped_gemm.
+ */
+int nvfp4_grouped_gemm_batched(int problem_count, const int *group_counts,
+                               const nvfp4_problem_size *problem_sizes,
+                               const void *const *A, const void *const *B,
+                               const void *const *SFA, const void *const *SFB,
+                               void *const *C, nvfp4_stream_t stream);
+
+/*
  * nvfp4_grouped_gemm_device -- nvfp4_grouped_gemm with the group table in
  * DEVICE memory, so that the sizes and pointers can come from an earlier
  * kernel (a mixture-of-experts router) without a host round trip, and so that

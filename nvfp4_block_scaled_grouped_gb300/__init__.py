@@ -9,6 +9,8 @@ The functions mirror the C entry points:
 
 * :func:`grouped_gemm` -- ``nvfp4_grouped_gemm`` (raw device pointers);
 * :func:`grouped_gemm_tensors` -- the same call taking torch CUDA tensors;
+* :func:`grouped_gemm_batched` -- ``nvfp4_grouped_gemm_batched`` (several
+  grouped problems, one launch);
 * :func:`grouped_gemm_device` / :class:`DeviceGroupTable` --
   ``nvfp4_grouped_gemm_device`` (group table in device memory);
 * :func:`pack_scales` / :func:`scale_bytes` -- the scale-layout packer;
@@ -23,7 +25,8 @@ import threading
 from pathlib import Path
 
 __all__ = [
-    "Nvfp4Error", "lib", "library_path", "grouped_gemm", "grouped_gemm_tensors", "grouped_gemm_device",
+    "Nvfp4Error", "lib", "library_path", "grouped_gemm", "grouped_gemm_tensors", "grouped_gemm_batched",
+    "grouped_gemm_device",
     "DeviceGroupTable", "quantize_pack", "quantize_pack_tensor", "DTYPE_BF16", "DTYPE_F16", "pack_scales",
     "pack_scales_tensor", "scale_bytes", "device_status", "set_tile_n", "MAX_GROUPS", "STATUS",
 ]
@@ -66,6 +69,9 @@ def lib() -> ctypes.CDLL:
         vp, vpp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)
         L.nvfp4_grouped_gemm.restype = ctypes.c_int
         L.nvfp4_grouped_gemm.argtypes = [ctypes.c_int, ctypes.POINTER(ProblemSize), vpp, vpp, vpp, vpp, vpp, vp]
+        L.nvfp4_grouped_gemm_batched.restype = ctypes.c_int
+        L.nvfp4_grouped_gemm_batched.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ProblemSize),
+                                                 vpp, vpp, vpp, vpp, vpp, vp]
         L.nvfp4_grouped_gemm_device.restype = ctypes.c_int
         L.nvfp4_grouped_gemm_device.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, vp, vp]
         L.nvfp4_quantize_pack.restype = ctypes.c_int
@@ -116,6 +122,27 @@ def grouped_gemm(problem_sizes, A, B, SFA, SFB, C, stream=None, *, check: bool =
         sizes[g] = ProblemSize(int(m), int(n), int(k), int(l))
     status = lib().nvfp4_grouped_gemm(
         G, sizes, _ptr_array(A), _ptr_array(B), _ptr_array(SFA), _ptr_array(SFB), _ptr_array(C),
+        ctypes.c_void_p(_stream_handle(stream) or None))
+    if check:
+        _check(status)
+    return status
+
+
+def grouped_gemm_batched(problems, stream=None, *, check: bool = True) -> int:
+    """nvfp4_grouped_gemm_batched: `problems` is a list of (problem_sizes, A,
+    B, SFA, SFB, C) tuples with host lists of device addresses (ints), one
+    per independent grouped problem; all run in one launch."""
+    counts = (ctypes.c_int * max(len(problems), 1))(*[len(p[0]) for p in problems])
+    flat = [[], [], [], [], [], []]
+    for p in problems:
+        for i in range(6):
+            flat[i].extend(p[i])
+    G = len(flat[0])
+    sizes = (ProblemSize * max(G, 1))()
+    for g, (m, n, k, l) in enumerate(flat[0]):
+        sizes[g] = ProblemSize(int(m), int(n), int(k), int(l))
+    status = lib().nvfp4_grouped_gemm_batched(
+        len(problems), counts, sizes, *[_ptr_array(flat[i]) for i in range(1, 6)],
         ctypes.c_void_p(_stream_handle(stream) or None))
     if check:
         _check(status)

@@ -426,6 +426,26 @@ int nvfp4_grouped_gemm(int group_count, const nvfp4_problem_size *problem_sizes,
                                &w->state, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int nvfp4_grouped_gemm_batched(int problem_count, const int *group_counts, const nvfp4_problem_size *problem_sizes,
+                               const void *const *A, const void *const *B, const void *const *SFA,
+                               const void *const *SFB, void *const *C, nvfp4_stream_t stream) {
+    if (problem_count < 0)
+        return fail(NVFP4_ERR_INVALID_ARG, "problem_count %d < 0", problem_count);
+    if (problem_count == 0)
+        return NVFP4_OK;
+    if (!group_counts)
+        return fail(NVFP4_ERR_INVALID_ARG, "null group_counts");
+    long long total = 0;
+    for (int p = 0; p < problem_count; ++p) {
+        if (group_counts[p] < 0)
+            return fail(NVFP4_ERR_INVALID_ARG, "problem %d: group count %d < 0", p, group_counts[p]);
+        total += group_counts[p];
+    }
+    if (total > NVFP4_MAX_GROUPS)
+        return fail(NVFP4_ERR_INVALID_ARG, "%lld groups in all; at most %d fit one launch", total, NVFP4_MAX_GROUPS);
+    return nvfp4_grouped_gemm((int)total, problem_sizes, A, B, SFA, SFB, C, stream);
+}
+
 int nvfp4_grouped_gemm_device(int group_count, const nvfp4_problem_size *problem_sizes, const void *const *A,
                               const void *const *B, const void *const *SFA, const void *const *SFB, void *const *C,
                               nvfp4_stream_t stream) {

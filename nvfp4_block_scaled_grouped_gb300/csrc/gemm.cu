@@ -887,15 +887,36 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 const uint8_t *st_sfb = st_sfa + C::kSfaBytes;
                 const uint32_t sfa_t = tmem_base + quarter + (uint32_t)(C::kSfColBase + stage * C::kSfColsPerStage);
                 const uint32_t sfb_t = sfa_t + C::kSfaCols;
-                for (int kb = 0; kb < nkb; ++kb) {
-                    ptx::tmem_st_32x32b_x4(sfa_t + 4 * kb,
-                                           *reinterpret_cast<const uint4 *>(st_sfa + kb * kSfAtomBytes + 16 * lane));
+                // The stage's SFA columns (4 per k-block) and SFB columns
+                // (BN/32 per k-block) are each one contiguous run: all of a
+                // lane's words go out in one wide store per operand. Columns
+                // of k-blocks past the K tail get zeros (no MMA reads them).
+                uint32_t va[C::kSfaCols], vb[C::kSfbCols];
 #pragma unroll
-                    for (int j = 0; j < C::kSfbRowBlocks; ++j)
-                        ptx::tmem_st_32x32b_x4(sfb_t + kb * (BN / 32) + 4 * j,
-                                               *reinterpret_cast<const uint4 *>(
-                                                   st_sfb + (j * 4 + kb) * kSfAtomBytes + 16 * lane));
+                for (int kb = 0; kb < 4; ++kb) {
+                    const uint4 w = kb < nkb ? *reinterpret_cast<const uint4 *>(st_sfa + kb * kSfAtomBytes + 16 * lane)
+                                             : make_uint4(0, 0, 0, 0);
+                    va[4 * kb] = w.x;
+                    va[4 * kb + 1] = w.y;
+                    va[4 * kb + 2] = w.z;
+                    va[4 * kb + 3] = w.w;
+#pragma unroll
+                    for (int j = 0; j < C::kSfbRowBlocks; ++j) {
+                        const uint4 u = kb < nkb ? *reinterpret_cast<const uint4 *>(
+                                                       st_sfb + (j * 4 + kb) * kSfAtomBytes + 16 * lane)
+                                                 : make_uint4(0, 0, 0, 0);
+                        const int c = kb * (BN / 32) + 4 * j;
+                        vb[c] = u.x;
+                        vb[c + 1] = u.y;
+                        vb[c + 2] = u.z;
+                        vb[c + 3] = u.w;
+                    }
                 }
+                ptx::tmem_st_32x32b_x16(sfa_t, va);
+                if constexpr (C::kSfbCols == 32)
+                    ptx::tmem_st_32x32b_x32(sfb_t, vb);
+                else
+                    ptx::tmem_st_32x32b_x16(sfb_t, reinterpret_cast<const uint32_t(&)[16]>(vb));
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 __syncwarp();

@@ -88,6 +88,19 @@ def test_device_table_host_argument_errors(L):
     assert f(2, vp(0x20000), vp(0x10004), *arrays[1:], None) == -3             # pointer array not 8-byte aligned
 
 
+def test_batched_call_host_argument_errors(L):
+    f = L.nvfp4_grouped_gemm_batched
+    counts = (ctypes.c_int * 3)(2, -1, 1)
+    assert f(0, None, None, None, None, None, None, None, None) == 0       # no problems: no-op
+    assert f(-1, None, None, None, None, None, None, None, None) == -1
+    assert f(2, None, None, None, None, None, None, None, None) == -1      # null counts
+    assert f(3, counts, None, None, None, None, None, None, None) == -1    # negative count
+    big = (ctypes.c_int * 2)(300, 213)
+    assert f(2, big, None, None, None, None, None, None, None) == -1       # 513 groups
+    zero = (ctypes.c_int * 2)(0, 0)
+    assert f(2, zero, None, None, None, None, None, None, None) == 0       # only empty problems
+
+
 def test_quantize_pack_host_argument_errors(L):
     vp = ctypes.c_void_p
     f = L.nvfp4_quantize_pack
