@@ -87,21 +87,32 @@ def roofline_terms(flops, nbytes, peaks):
     return ("tensor" if t_flop >= t_mem else "hbm"), t_flop, t_mem, fp4_tflops
 
 
+def kernel_code_digest(path) -> str:
+    """sha256[:16] of a CUDA source with // comments and blank lines removed
+    (an edit of comments alone does not change the kernel)."""
+    import hashlib
+    import re
+    lines = []
+    for line in Path(path).read_text().splitlines():
+        line = re.sub(r"//.*$", "", line).rstrip()
+        if line.strip():
+            lines.append(line)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def stored_traffic(workload, tile_n):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the kernel source as it is now (else None)."""
-    import hashlib
+    the kernel code as it is now (else None)."""
     summ = ROOT / "profiles" / f"gemm_kernel_{workload}.txt"
     if not summ.exists():
         return None
-    src = ROOT / "nvfp4_block_scaled_grouped_gb300" / "csrc" / "gemm.cu"
-    digest = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    digest = kernel_code_digest(ROOT / "nvfp4_block_scaled_grouped_gb300" / "csrc" / "gemm.cu")
     kv = {}
     for line in summ.read_text().splitlines():
-        if ":" in line:
-            k, v = line.split(":", 1)
+        if ": " in line:
+            k, v = line.split(": ", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("gemm.cu sha256[:16]") != digest or kv.get("tile_n") != str(tile_n):
+    if kv.get("gemm.cu code sha256[:16]", "").split(" ")[0] != digest or kv.get("tile_n") != str(tile_n):
         return None
     try:
         return float(kv["dram bytes per launch"])

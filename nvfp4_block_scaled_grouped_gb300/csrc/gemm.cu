@@ -1,40 +1,47 @@
 // gemm.cu -- the grouped NVFP4 block-scaled GEMM for sm_103a.
 //
-// One persistent kernel per call, grouped_gemm_kernel<BN, CAP> (one CTA per
-// SM, 320 threads, cooperative launch so every CTA is resident). The group
-// table (sizes and pointers of up to CAP groups) arrives as a __grid_constant__
-// kernel parameter, and at start-up every CTA
+// One persistent kernel per call, grouped_gemm_kernel<BN, CAP, DEV> (one CTA
+// per SM, 320 threads, cooperative launch so every CTA is resident). The group
+// table (sizes, batch counts and pointers of up to CAP groups) arrives as a
+// __grid_constant__ kernel parameter, or (DEV) stays in the caller's device
+// arrays and is read, and checked, by the kernel. At start-up every CTA
 //   * computes the per-group output-tile counts and schedule-unit counts and
-//     their exclusive prefix sums (one warp scan; the tile prefix sum that the
-//     "nvfp4 group gemm" submissions build on the host is built here), and
+//     their exclusive prefix sums (the tile prefix sum that the "nvfp4 group
+//     gemm" submissions build on the host is built here), and from them the
+//     schedule when the host could not choose it (DEV);
 //   * patches the TMA descriptors of its share of the groups (group g by CTA
 //     g mod gridDim) from a host-encoded template with tensormap.replace,
-//     releases them and bumps a publication counter; producers wait for the
-//     counter before their first copy (the per-group descriptor patching of
+//     releases them and adds 1 to a publication counter; producers wait for
+//     all CTAs before their first copy (the per-group descriptor patching of
 //     submission 506336, TMA warp, and the descriptor initialisation kernel of
-//     submission 499344, done inside the one launch).
+//     submission 499344, done inside the one launch). The last producer past
+//     that wait resets the call counters for the next call.
 // Roles:
 //       warp 4    TMA producer: A and B tiles (128-byte swizzle) plus the scale
 //                 runs of each 256-K k-tile (1-D bulk copies: a 128-row x 256-K
 //                 slice of the reordered scale layout is 4 consecutive 512-byte
 //                 atoms) into a multi-stage shared-memory ring;
 //       warps 6-9 scale writers: each copies the stage's scale atoms into its
-//                 own 32-lane quarter of TMEM with tcgen05.st (the layout the
-//                 block-scaled MMA reads: lane l, column c of a k-block holds
-//                 the 4 scales of row 32c + l, the same in every quarter);
+//                 own 32-lane quarter of TMEM with two wide tcgen05.st (the
+//                 layout the block-scaled MMA reads: lane l, column c of a
+//                 k-block holds the 4 scales of row 32c + l, the same in every
+//                 quarter);
 //       warp 5    MMA issuer: tcgen05.mma kind::mxf4nvf4 block_scale
 //                 (scale_vec::4X = one e4m3 scale per 16 elements),
 //                 128 x BN x 64, four per k-tile, into a TMEM accumulator;
 //                 commits free the smem stage and publish the accumulator;
-//       warps 0-3 epilogue: tcgen05.ld of the accumulator lanes they own,
-//                 fp32 -> fp16 round-to-nearest-even, staged through a
-//                 swizzled per-warp buffer so each store writes 8 rows x 64 B;
-//                 rows >= m and column chunks >= n skipped.
+//       warps 0-3 epilogue of every segment but the CTA's last: tcgen05.ld of
+//                 the accumulator lanes they own, fp32 -> fp16
+//                 round-to-nearest-even, staged through a swizzled per-warp
+//                 buffer so each store writes 8 rows x 64 B; rows >= m and
+//                 column chunks >= n skipped;
+//       warps 0-7 epilogue of the CTA's last segment, once every role has
+//                 left its loop (the last epilogue is on the critical path).
 //
 // Schedule. The work of a call is a sequence of schedule units: for every
-// output tile (group-major, M fastest inside a group, so neighbouring units
-// share a B panel) its k-tiles, at least one per tile (a k == 0 tile has one
-// unit and produces zeros). CTAs take
+// output tile (group-major, batch-major inside a group, then M fastest, so
+// neighbouring units share a B panel) its k-tiles, at least one per tile (a
+// k == 0 tile has one unit and produces zeros). CTAs take
 //   * whole tiles round-robin (tile blockIdx.x, + gridDim.x, ...) when there
 //     are many tiles per SM, so the CTAs running at one time work on
 //     neighbouring tiles and share their A and B panels in L2;
@@ -43,8 +50,9 @@
 //     tile's first k-tile finishes it; every later piece is the first segment
 //     of its CTA, so it is computed without waiting, stored as an fp32 partial
 //     tile in the CTA's workspace slot and published with an epoch flag
-//     (release); the finishing CTA acquires the flags, adds the partials and
-//     writes C.
+//     (release); the finishing CTA's producer acquires the flags and copies
+//     the next piece's partial tile into the ring as the final MMAs free it,
+//     and the last epilogue adds it (any further pieces from L2).
 //
 // Every wait is bounded (%globaltimer): a wait that gives up sets a bit in
 // the workspace status word and a CTA-wide abort flag, the other roles leave

@@ -74,3 +74,30 @@ def test_reference_arm_prints_on_rank_zero_only(rank):
         assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
     else:
         assert lines == []
+
+
+def test_profile_summary_lookup(tmp_path, monkeypatch):
+    """The roofline's `traffic` comes from a committed ncu summary only when
+    the summary names the kernel code as it is now (comments do not count)."""
+    sys.path.insert(0, str(ROOT))
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_text("int x; // a comment\n\n__global__ void k() {}\n")
+    d = bench.kernel_code_digest(src)
+    src.write_text("int x; // another comment\n// more\n__global__ void k() {}\n")
+    assert bench.kernel_code_digest(src) == d
+    src.write_text("int y;\n__global__ void k() {}\n")
+    assert bench.kernel_code_digest(src) != d
+    cur = bench.kernel_code_digest(ROOT / "nvfp4_block_scaled_grouped_gb300" / "csrc" / "gemm.cu")
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "nvfp4_block_scaled_grouped_gb300" / "csrc").mkdir(parents=True)
+    (tmp_path / "nvfp4_block_scaled_grouped_gb300" / "csrc" / "gemm.cu").write_text(
+        (ROOT / "nvfp4_block_scaled_grouped_gb300" / "csrc" / "gemm.cu").read_text())
+    summ = tmp_path / "profiles" / "gemm_kernel_decode.txt"
+    summ.write_text(f"gemm.cu code sha256[:16]: {cur} (comments and blank lines stripped)\ntile_n: 256\n"
+                    "dram bytes per launch: 123456\n")
+    monkeypatch.setattr(bench, "ROOT", tmp_path)
+    assert bench.stored_traffic("decode", 256) == 123456.0
+    assert bench.stored_traffic("decode", 128) is None
+    summ.write_text("gemm.cu code sha256[:16]: 0000000000000000\ntile_n: 256\ndram bytes per launch: 1\n")
+    assert bench.stored_traffic("decode", 256) is None
