@@ -141,12 +141,15 @@ int stream_workspace(int device, cudaStream_t stream, int slots, StreamWorkspace
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Bound of every wait in the GEMM kernel: NVFP4_WATCHDOG_MS milliseconds
+// (fractions allowed), default 4000.
 uint64_t watchdog_ns() {
     const char *s = std::getenv("NVFP4_WATCHDOG_MS");
-    long long ms = s ? std::atoll(s) : 0;
-    if (ms <= 0)
-        ms = 4000;
-    return (uint64_t)ms * 1000000ull;
+    double ms = s ? std::strtod(s, nullptr) : 0.0;
+    if (!(ms > 0.0) || ms > 3.6e6)
+        ms = 4000.0;
+    const double ns = ms * 1e6;
+    return ns < 1.0 ? 1ull : (uint64_t)ns;
 }
 
 // BLOCK_N for a call: an explicit nvfp4_set_tile_n() value or NVFP4_TILE_N,

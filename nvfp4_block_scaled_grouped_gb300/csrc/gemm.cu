@@ -92,7 +92,7 @@ struct Cfg {
     static_assert(kSfColBase + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
     static constexpr int kThreads = 320;                           // 10 warps
     static constexpr int kBarrierBytes = 384;
-    static_assert((3 * kStages + 2 * kAccStages) * 8 <= 184, "barrier area");
+    static_assert((3 * kStages + 2 * kAccStages) * 8 <= 176, "barrier area");
     static constexpr int kEpiStageBytes = 32 * 64;                 // per epilogue warp: 32 rows x 32 fp16
     // A finishing CTA receives the next piece's partial tile in ring stages,
     // kPartialChunksPerStage 16 KiB chunks (32 columns x 128 rows fp32) per
@@ -507,7 +507,12 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     auto sff_bar = [&](int s) { return bars + 8u * (2 * C::kStages + s); };
     auto accf_bar = [&](int a) { return bars + 8u * (3 * C::kStages + a); };
     auto acce_bar = [&](int a) { return bars + 8u * (3 * C::kStages + C::kAccStages + a); };
+    const uint32_t drain_bar = bars + 176;    // the MMA thread's issued MMAs have completed
     const uint32_t partial_bar = bars + 184;  // partial tile of a split tile landed in smem
+    // Bound of the waits that let this CTA's own asynchronous copies and MMAs
+    // finish before it frees TMEM and exits: never shorter than 1 s, whatever
+    // the watchdog, so an abort never leaves work in flight.
+    const uint64_t drain_ns = p.timeout_ns > 1000000000ull ? p.timeout_ns : 1000000000ull;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_area + 192);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 196);
     volatile int *s_epi_ok = reinterpret_cast<volatile int *>(bar_area + 208);  // [3]: by segment parity, tail
@@ -535,6 +540,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 ptx::mbar_init(acce_bar(a), 4);
             }
             ptx::mbar_init(partial_bar, 1);
+            ptx::mbar_init(drain_bar, 1);
             *abort_flag = 0;
             s_tail->valid = 0;
             s_tail->part_state = 0;
@@ -805,7 +811,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                         continue;
                     const uint32_t par = (armed_parity >> s) & 1u;
                     const uint64_t t0 = ptx::globaltimer();
-                    while (!ptx::mbar_try_wait(full_bar(s), par) && ptx::globaltimer() - t0 < p.timeout_ns) {
+                    while (!ptx::mbar_try_wait(full_bar(s), par) && ptx::globaltimer() - t0 < drain_ns) {
                     }
                 }
             }
@@ -861,6 +867,13 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                     acc = 0;
                     acc_phase ^= 1u;
                 }
+            }
+            // Every MMA this thread issued completes before the CTA can free
+            // TMEM -- on the normal path the epilogue already waits for them,
+            // after an abort nothing else would.
+            ptx::tc_commit(drain_bar);
+            const uint64_t t0 = ptx::globaltimer();
+            while (!ptx::mbar_try_wait(drain_bar, 0) && ptx::globaltimer() - t0 < drain_ns) {
             }
         }
     } else if (warp >= 6) {
@@ -1017,7 +1030,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 // after an abort
                 const uint64_t t0 = ptx::globaltimer();
                 bool landed;
-                while (!(landed = ptx::mbar_try_wait(partial_bar, 0)) && ptx::globaltimer() - t0 < p.timeout_ns) {
+                while (!(landed = ptx::mbar_try_wait(partial_bar, 0)) && ptx::globaltimer() - t0 < drain_ns) {
                 }
                 if (!landed) {
                     *abort_flag = 1;
