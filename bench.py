@@ -312,18 +312,27 @@ def gpu_arm(args, rank, world, local_rank):
     dp = DeviceProblem(problem_sizes=[s for d in dps for s in d.problem_sizes], A=[t for d in dps for t in d.A],
                        B=[t for d in dps for t in d.B], SFA=[t for d in dps for t in d.SFA],
                        SFB=[t for d in dps for t in d.SFB], C=[t for d in dps for t in d.C])
-    if len(dps) > 1:
+    counts = [len(d.problem_sizes) for d in dps]
+
+    def make_call(q):
+        """The timed call on operands q (a DeviceProblem), through the chosen entry point."""
         ptr = lambda t: 0 if t.numel() == 0 else int(t.data_ptr())
-        batch = [(d.problem_sizes, [ptr(t) for t in d.A], [ptr(t) for t in d.B], [ptr(t) for t in d.SFA],
-                  [ptr(t) for t in d.SFB], [ptr(t) for t in d.C]) for d in dps]
-        call = lambda: nv.grouped_gemm_batched(batch, stream)
-    elif args.api == "device":
-        table = nv.DeviceGroupTable(len(dp.problem_sizes), device=dev)
-        table.set(dp.problem_sizes, dp.A, dp.B, dp.SFA, dp.SFB, dp.C)
-        torch.cuda.synchronize()
-        call = lambda: table.run(stream)
-    else:
-        call = lambda: dp.run(stream)
+        if len(counts) > 1:
+            batch, at = [], 0
+            for c in counts:
+                sl = slice(at, at + c)
+                batch.append((q.problem_sizes[sl], [ptr(t) for t in q.A[sl]], [ptr(t) for t in q.B[sl]],
+                              [ptr(t) for t in q.SFA[sl]], [ptr(t) for t in q.SFB[sl]], [ptr(t) for t in q.C[sl]]))
+                at += c
+            return lambda: nv.grouped_gemm_batched(batch, stream)
+        if args.api == "device":
+            table = nv.DeviceGroupTable(len(q.problem_sizes), device=dev)
+            table.set(q.problem_sizes, q.A, q.B, q.SFA, q.SFB, q.C)
+            torch.cuda.synchronize()
+            return lambda: table.run(stream)
+        return lambda: q.run(stream)
+
+    call = make_call(dp)
 
     # L2 flush: read a buffer 4x the 129 MB L2 (reads leave no dirty lines to write back)
     flush = torch.ones(args.flush_mb << 18, dtype=torch.int32, device=dev)
@@ -365,39 +374,54 @@ def gpu_arm(args, rank, world, local_rank):
     t_max = max_over_ranks(t_ms, world, dev)
     value = replica_throughput(flops, world, t_max * 1e-3) / 1e12
 
-    # ---- e2e: host buffers in pinned memory, copies inside the timed region
+    # ---- e2e: host buffers in pinned memory, copies inside the timed region.
+    # The inputs of a step live in one pinned host blob and the outputs come
+    # back into another: one H2D and one D2H copy per step, the call on
+    # device views of the blobs.
     e2e = None
     if not args.no_e2e:
-        host_in = []
-        dev_in = []
-        for lst in (dp.A, dp.B, dp.SFA, dp.SFB):
-            for t in lst:
-                if t.numel():
-                    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                    h.copy_(t)
-                    host_in.append(h)
-                    dev_in.append(t)
-        host_out = [torch.empty(c.shape, dtype=c.dtype, pin_memory=True) for c in dp.C]
-        h2d = sum(h.numel() * h.element_size() for h in host_in)
-        d2h = sum(h.numel() * h.element_size() for h in host_out)
+        def blob(tensors):
+            offs, pos = [], 0
+            for t in tensors:
+                offs.append(pos)
+                pos += -(-t.numel() * t.element_size() // 256) * 256
+            return offs, max(pos, 256)
+        ins = [dp.A, dp.B, dp.SFA, dp.SFB]
+        flat_in = [t for lst in ins for t in lst]
+        in_offs, in_bytes = blob(flat_in)
+        out_offs, out_bytes = blob(dp.C)
+        d_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+        h_in = torch.empty(in_bytes, dtype=torch.uint8, pin_memory=True)
+        d_out = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+        h_out = torch.empty(out_bytes, dtype=torch.uint8, pin_memory=True)
+
+        def view(base, off, t):
+            n = t.numel() * t.element_size()
+            return base[off:off + n].view(t.dtype).view(t.shape)
+        views = [view(d_in, o, t) for o, t in zip(in_offs, flat_in)]
+        for v, t in zip(views, flat_in):
+            v.copy_(t)
+        h_in.copy_(d_in)
+        it = iter(views)
+        q = DeviceProblem(problem_sizes=dp.problem_sizes, A=[next(it) for _ in dp.A], B=[next(it) for _ in dp.B],
+                          SFA=[next(it) for _ in dp.SFA], SFB=[next(it) for _ in dp.SFB],
+                          C=[view(d_out, o, c) for o, c in zip(out_offs, dp.C)])
+        call_e2e = make_call(q)
+        h2d, d2h = in_bytes, out_bytes
         e2e_steps = max(3, min(args.steps, 10))
         for _ in range(2):
-            for h, d in zip(host_in, dev_in):
-                d.copy_(h, non_blocking=True)
-            call()
-            for h, c in zip(host_out, dp.C):
-                h.copy_(c, non_blocking=True)
+            d_in.copy_(h_in, non_blocking=True)
+            call_e2e()
+            h_out.copy_(d_out, non_blocking=True)
         torch.cuda.synchronize()
         e_ms = []
         for _ in range(e2e_steps):
             flush.sum()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            for h, d in zip(host_in, dev_in):
-                d.copy_(h, non_blocking=True)
-            call()
-            for h, c in zip(host_out, dp.C):
-                h.copy_(c, non_blocking=True)
+            d_in.copy_(h_in, non_blocking=True)
+            call_e2e()
+            h_out.copy_(d_out, non_blocking=True)
             b.record(stream)
             b.synchronize()
             e_ms.append(a.elapsed_time(b))
