@@ -214,25 +214,15 @@ int check_groups(int group_count, int max_groups, const nvfp4_problem_size *prob
 
 int current_block_n() { return choose_block_n(); }
 
-// NVFP4_SPLIT forces the schedule: -1 if unset (automatic), else 0 or 1.
+// NVFP4_SPLIT forces the schedule: -1 if unset (automatic), else 0 (whole
+// tiles), 1 (all tiles in the split range) or 2 (whole waves + split rest).
 int split_override() {
     const char *s = std::getenv("NVFP4_SPLIT");
-    if (s && *s)
-        return std::atoi(s) != 0 ? 1 : 0;
+    if (s && *s) {
+        const int v = std::atoi(s);
+        return v == 1 ? 1 : (v == 2 ? 2 : 0);
+    }
     return -1;
-}
-
-// Split (stream-K) schedules pay off when whole tiles leave the last wave
-// mostly idle: ceil(T / P) waves against T / P waves of work. They cost
-// partial-tile traffic and an extra epilogue per split tile, so they are used
-// only when whole tiles would waste at least ~30% of the time (the kernel
-// applies the same integer rule to device-table calls).
-bool want_split(long long total_tiles, int sm_count) {
-    const int forced = split_override();
-    if (forced >= 0)
-        return forced != 0;
-    const long long waves = (total_tiles + sm_count - 1) / sm_count;
-    return 10ll * waves * sm_count >= 14ll * total_tiles;
 }
 
 // Whether `stream` is capturing into a CUDA graph (the launch is then
@@ -274,11 +264,18 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
         if (s != NVFP4_OK)
             return s;
         const int sms = st->sm_count;
-        cfg.split = (partial_slots >= sms && want_split(total_tiles, sms)) ? 1 : 0;
-        if (cfg.split)
+        int forced = split_override();
+        if (partial_slots < sms)
+            forced = 0;  // no partial-tile slots: whole tiles only
+        const int split_tile = choose_split_tile((int)total_tiles, sms, forced);
+        cfg.split = split_tile < total_tiles ? 1 : 0;
+        cfg.split_tile = split_tile;
+        if (!cfg.split)
+            cfg.grid = (int)(total_tiles < sms ? total_tiles : sms);
+        else if (split_tile == 0)
             cfg.grid = (int)(total_work < sms ? total_work : sms);
         else
-            cfg.grid = (int)(total_tiles < sms ? total_tiles : sms);
+            cfg.grid = sms;  // whole waves use every SM
         if (group_count > kMediumGroups && prefix_slots < cfg.grid)
             return fail(NVFP4_ERR_UNSUPPORTED, "workspace has %d CTA slots, the launch needs %d", prefix_slots,
                         cfg.grid);
@@ -353,7 +350,8 @@ int launch_device_table(int group_count, const DeviceTable &dt, int block_n, voi
     cfg.total_tiles = 0;              // derived by the kernel
     cfg.total_work = 0;
     cfg.grid = st->sm_count < slots ? st->sm_count : slots;
-    cfg.split = split_override();
+    cfg.split = split_override();  // the kernel chooses with the same rule
+    cfg.split_tile = 0;
     cfg.capacity = capacity;
     cfg.timeout_ns = watchdog_ns();
     cfg.device_table = true;

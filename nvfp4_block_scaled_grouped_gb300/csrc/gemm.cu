@@ -117,7 +117,7 @@ struct GemmParams {
     alignas(64) uint8_t tmpl_b[128];
     WorkspaceView ws;
     DeviceTable dt;
-    int32_t group_count, block_n, total_tiles, total_work, split, desc_maps;
+    int32_t group_count, block_n, total_tiles, total_work, split, split_tile, desc_maps;
     uint64_t timeout_ns;
     GroupArgs groups[DEV ? 1 : CAP];
 };
@@ -262,65 +262,89 @@ struct Segment {
     int w_tile_end;  // schedule index one past the tile's last unit
 };
 
-// Whether a split schedule pays for T tiles on P CTAs: whole tiles would take
-// ceil(T / P) waves for T / P waves of work, and 1.4x is the break-even point
-// (the host applies the same integer rule).
-__device__ __forceinline__ bool split_pays(int T, int P) {
-    const long long waves = (T + P - 1) / P;
-    return 10ll * waves * P >= 14ll * T;
-}
-
 // First schedule unit of CTA c out of p in a split (stream-K) schedule.
 __device__ __forceinline__ int split_begin(int c, int p, int total_work) {
     return (int)(((long long)c * total_work) / p);
 }
 
-// The sequence of segments one CTA processes; every role walks the same one.
+// The sequence of segments one CTA processes; every role walks the same one:
+// first the head of its split range when that range starts inside a tile (a
+// later piece of a split tile, computed before anything else so its partial
+// tile is published early), then its whole tiles (blockIdx, + P, ... below
+// the first split tile), then the rest of its split range (ending, when the
+// range ends inside a tile, with that tile's first piece, which this CTA
+// finishes as its last segment).
 template <int BN, int CAP, bool DEV>
 struct Cursor {
     const int32_t *prefix, *wprefix;
     const GemmParams<CAP, DEV> *prm;
-    int group_count, split;
-    int w, w_end;                 // split schedule: contiguous schedule units
-    int tile, total_tiles, step;  // whole-tile schedule: round-robin tiles
+    int group_count;
+    int tile, tile_end, step;  // whole tiles
+    int w, head_end, w_end;    // split range [w, w_end) of schedule units; head [w, head_end)
+    int phase;                 // 0: head, 1: whole tiles, 2: rest of the split range
+
+    __device__ __forceinline__ void split_segment(Segment &s, const int limit) {
+        s.g = find_group(wprefix, group_count, w);
+        const GInfo gi = group_info<BN>(load_group(*prm, s.g));
+        const int local = w - wprefix[s.g];
+        const int t = local / gi.work_tiles;
+        s.ktg = gi.work_tiles;
+        s.kt0 = local - t * gi.work_tiles;
+        const int rest = limit - w;
+        s.kt1 = s.kt0 + ((s.ktg - s.kt0) < rest ? (s.ktg - s.kt0) : rest);
+        s.b = t / gi.tiles_mn;
+        const int tb = t - s.b * gi.tiles_mn;
+        s.tm = tb % gi.tiles_m;
+        s.tn = tb / gi.tiles_m;
+        s.w_tile_end = wprefix[s.g] + (t + 1) * s.ktg;
+        w += s.kt1 - s.kt0;
+    }
 
     __device__ __forceinline__ bool next(Segment &s) {
-        int t;
-        if (split) {
-            if (w >= w_end)
-                return false;
-            s.g = find_group(wprefix, group_count, w);
-            const GInfo gi = group_info<BN>(load_group(*prm, s.g));
-            const int local = w - wprefix[s.g];
-            t = local / gi.work_tiles;
-            s.ktg = gi.work_tiles;
-            s.kt0 = local - t * gi.work_tiles;
-            const int rest = w_end - w;
-            s.kt1 = s.kt0 + ((s.ktg - s.kt0) < rest ? (s.ktg - s.kt0) : rest);
-            s.b = t / gi.tiles_mn;
-            const int tb = t - s.b * gi.tiles_mn;
-            s.tm = tb % gi.tiles_m;
-            s.tn = tb / gi.tiles_m;
-            w += s.kt1 - s.kt0;
-        } else {
-            if (tile >= total_tiles)
-                return false;
-            s.g = find_group(prefix, group_count, tile);
-            const GInfo gi = group_info<BN>(load_group(*prm, s.g));
-            t = tile - prefix[s.g];
-            s.b = t / gi.tiles_mn;
-            const int tb = t - s.b * gi.tiles_mn;
-            s.tm = tb % gi.tiles_m;
-            s.tn = tb / gi.tiles_m;
-            s.ktg = gi.work_tiles;
-            s.kt0 = 0;
-            s.kt1 = s.ktg;
-            tile += step;
+        if (phase == 0) {
+            if (w < head_end) {
+                split_segment(s, head_end);
+                return true;
+            }
+            phase = 1;
         }
-        s.w_tile_end = wprefix[s.g] + (t + 1) * s.ktg;
-        return true;
+        if (phase == 1) {
+            if (tile < tile_end) {
+                s.g = find_group(prefix, group_count, tile);
+                const GInfo gi = group_info<BN>(load_group(*prm, s.g));
+                const int t = tile - prefix[s.g];
+                s.b = t / gi.tiles_mn;
+                const int tb = t - s.b * gi.tiles_mn;
+                s.tm = tb % gi.tiles_m;
+                s.tn = tb / gi.tiles_m;
+                s.ktg = gi.work_tiles;
+                s.kt0 = 0;
+                s.kt1 = s.ktg;
+                s.w_tile_end = wprefix[s.g] + (t + 1) * s.ktg;
+                tile += step;
+                return true;
+            }
+            phase = 2;
+        }
+        if (w < w_end) {
+            split_segment(s, w_end);
+            return true;
+        }
+        return false;
     }
 };
+
+// Schedule unit index of the first unit of tile `tile` (total_work for
+// tile == total_tiles).
+template <int BN, int CAP, bool DEV>
+__device__ __forceinline__ int tile_first_unit(const GemmParams<CAP, DEV> &p, const int32_t *prefix,
+                                               const int32_t *wprefix, int group_count, int tile, int total_tiles,
+                                               int total_work) {
+    if (tile >= total_tiles)
+        return total_work;
+    const int g = find_group(prefix, group_count, tile);
+    return wprefix[g] + (tile - prefix[g]) * group_info<BN>(load_group(p, g)).work_tiles;
+}
 
 // What the epilogue does with a segment's accumulator.
 enum : int {
@@ -665,19 +689,41 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         ptx::tc_fence_after();
         tmem_base = *tmem_slot;
     }
-    // Schedule of the call: given by the host, or (device table) derived here
-    // by every CTA from the same prefix sums with the host's rule. A split
-    // schedule uses the first P CTAs.
+    // Schedule of the call (choose_split_tile): given by the host, or (device
+    // table) derived here by every CTA from the same prefix sums with the
+    // host's rule. Whole tiles go round-robin over P CTAs; the split range --
+    // the schedule units of tiles >= split_tile, from unit sk0 -- is cut into
+    // P equal parts. An all-split schedule uses the first P = min(units, grid)
+    // CTAs.
     const int total_tiles = DEV ? prefix[group_count] : p.total_tiles;
     const int total_work = DEV ? wprefix[group_count] : p.total_work;
-    int split = p.split;
-    if (DEV && split < 0)
-        split = (p.ws.partial_slots >= (int)gridDim.x && split_pays(total_tiles, (int)gridDim.x)) ? 1 : 0;
-    const int P = split ? (total_work < (int)gridDim.x ? total_work : (int)gridDim.x) : (int)gridDim.x;
-    const Cursor<BN, CAP, DEV> cursor0{prefix, wprefix, &p, group_count, split,
-                                       (int)blockIdx.x < P ? split_begin(blockIdx.x, P, total_work) : 0,
-                                       (int)blockIdx.x < P ? split_begin(blockIdx.x + 1, P, total_work) : 0,
-                                       (int)blockIdx.x, total_tiles, (int)gridDim.x};
+    int split_tile = p.split_tile;
+    if constexpr (DEV)
+        split_tile = choose_split_tile(total_tiles, (int)gridDim.x,
+                                       p.ws.partial_slots >= (int)gridDim.x ? p.split : 0);
+    const int split = split_tile < total_tiles ? 1 : 0;
+    const int P = (split && split_tile == 0 && total_work < (int)gridDim.x) ? total_work : (int)gridDim.x;
+    const int sk0 = tile_first_unit<BN>(p, prefix, wprefix, group_count, split_tile, total_tiles, total_work);
+    // first schedule unit of CTA c's part of the split range
+    auto sk_begin = [&](int c) { return sk0 + split_begin(c, P, total_work - sk0); };
+    Cursor<BN, CAP, DEV> cursor0{prefix, wprefix, &p, group_count, (int)blockIdx.x, split_tile, P, 0, 0, 0, 0};
+    if (split && (int)blockIdx.x < P) {
+        cursor0.w = sk_begin(blockIdx.x);
+        cursor0.w_end = sk_begin(blockIdx.x + 1);
+        cursor0.head_end = cursor0.w;
+        if (cursor0.w < cursor0.w_end) {
+            // the range starts inside a tile: that piece is the head
+            const int g = find_group(wprefix, group_count, cursor0.w);
+            const int wt = group_info<BN>(load_group(p, g)).work_tiles;
+            const int local = cursor0.w - wprefix[g];
+            if (local % wt != 0) {
+                const int tile_end_unit = cursor0.w + (wt - local % wt);
+                cursor0.head_end = tile_end_unit < cursor0.w_end ? tile_end_unit : cursor0.w_end;
+            }
+        }
+    }
+    if ((int)blockIdx.x >= P)
+        cursor0.tile = cursor0.tile_end;  // no whole tiles either
 
     if (warp == 4) {
         // ===================== TMA producer =====================
@@ -759,7 +805,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 // reading it have completed, oldest stage first.
                 const int cta = blockIdx.x;
                 int pieces = 0;
-                while (cta + pieces + 1 < P && split_begin(cta + pieces + 1, P, total_work) < sg.w_tile_end)
+                while (cta + pieces + 1 < P && sk_begin(cta + pieces + 1) < sg.w_tile_end)
                     ++pieces;
                 bool flags_ok = true;
                 for (int c2 = cta + 1; c2 <= cta + pieces && flags_ok; ++c2) {
@@ -1087,6 +1133,7 @@ cudaError_t launch_cap(const GemmLaunch &cfg, const GroupArgs *groups, const Wor
     prm.total_tiles = cfg.total_tiles;
     prm.total_work = cfg.total_work;
     prm.split = cfg.split;
+    prm.split_tile = cfg.split_tile;
     prm.desc_maps = cfg.desc_maps;
     prm.timeout_ns = cfg.timeout_ns;
     if constexpr (DEV) {

@@ -147,6 +147,32 @@ constexpr uint32_t kStatusDescTimeout = 16u;
 constexpr uint32_t kStatusBadGroup = 32u;  // a device-table group failed validation and was skipped
 constexpr uint32_t kStatusTimeoutMask = 31u;
 
+// Schedule of a call with T output tiles on P CTAs (the host applies it to
+// host-table calls, the kernel to device-table calls; integer arithmetic, so
+// both agree). Tiles [0, F) are whole tiles dealt round-robin; the schedule
+// units of tiles [F, T) are cut into P equal contiguous ranges, one per CTA
+// (stream-K: a tile may be split along K between consecutive CTAs). Returns
+// F (T: no split range). Automatic choice: 0 (all split) when whole tiles
+// would waste >= ~30% of the time in their last wave (ceil(T/P) >= 1.4 T/P),
+// else T. Splitting costs an fp32 partial tile per piece through the SM's
+// store port (about two fp16 epilogues), so the whole-waves-plus-split-rest
+// form (F = P * floor(T/P)) is measured slower than whole tiles on every
+// workload here and is only taken when forced.
+// `forced`: -1 automatic, 0 no split, 1 all split, 2 whole waves + split rest.
+__host__ __device__ inline int choose_split_tile(int T, int P, int forced) {
+    const int full = T / P, rem = T - full * P;
+    const long long waves = full + (rem ? 1 : 0);
+    if (forced == 0 || T == 0)
+        return T;
+    if (forced == 1)
+        return 0;
+    if (forced == 2)
+        return full * P;
+    if (rem != 0 && 10ll * waves * P >= 14ll * T)
+        return 0;
+    return T;
+}
+
 // Launch configuration chosen by the host for one call.
 struct GemmLaunch {
     int block_n;            // 128 or 256
@@ -155,8 +181,9 @@ struct GemmLaunch {
     int total_tiles;        // output tiles (host-table calls)
     int total_work;         // schedule units: sum over tiles of max(k-tiles, 1) (host-table calls)
     int grid;               // persistent CTAs (all resident: cooperative launch)
-    int split;              // 1: CTAs take equal ranges of schedule units (tiles may be split along K);
-                            // device-table calls: -1 = decided by the kernel, else forced
+    int split;              // 1: tiles >= split_tile form a split range (see choose_split_tile);
+                            // device-table calls: the `forced` argument of choose_split_tile
+    int split_tile;         // first tile of the split range (host-table calls)
     int capacity;           // workspace descriptor capacity (groups)
     uint64_t timeout_ns;    // bound of every wait
     bool device_table;      // the group table is `dt` (device memory), not the host array

@@ -61,7 +61,7 @@ EDGE_SIZES = [
 ]
 
 
-@pytest.mark.parametrize("block_n,split", [(128, None), (256, None), (256, "1"), (128, "0")])
+@pytest.mark.parametrize("block_n,split", [(128, None), (256, None), (256, "1"), (128, "0"), (256, "2")])
 def test_device_table_edge_shapes(nv, oracle_mod, monkeypatch, block_n, split):
     """The kernel reads sizes and pointers from device memory, derives the tile
     counts, prefix sums and the schedule itself (split forced either way or

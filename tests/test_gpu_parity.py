@@ -36,6 +36,8 @@ def _schedule(monkeypatch, split):
     or whole-tile schedule."""
     if split is None:
         monkeypatch.delenv("NVFP4_SPLIT", raising=False)
+    elif split == "hybrid":
+        monkeypatch.setenv("NVFP4_SPLIT", "2")   # whole tiles for the full waves, the rest split
     else:
         monkeypatch.setenv("NVFP4_SPLIT", "1" if split else "0")
 
@@ -94,7 +96,8 @@ EDGE_SIZES = [
 ]
 
 
-@pytest.mark.parametrize("block_n,split", [(128, False), (256, False), (128, True), (256, True)])
+@pytest.mark.parametrize("block_n,split", [(128, False), (256, False), (128, True), (256, True), (256, "hybrid"),
+                                           (128, "hybrid")])
 def test_edge_shapes_full(nv, oracle_mod, monkeypatch, block_n, split):
     """All edge shapes in one call; with the split schedule forced, the tiles
     are cut along K over many CTAs (most pieces one k-tile long), so the
@@ -201,7 +204,9 @@ def _workload(name):
 
 @pytest.mark.parametrize("name,block_n,split", [("decode", 256, None), ("decode", 128, False),
                                                 ("prefill", 256, None), ("prefill", 128, True),
-                                                ("ragged", 256, None), ("zipf64", 256, None)])
+                                                ("prefill", 256, "hybrid"), ("ragged", 256, None),
+                                                ("ragged", 256, "hybrid"), ("zipf64", 256, None),
+                                                ("zipf64", 256, "hybrid")])
 def test_full_size_sampled(nv, oracle_mod, monkeypatch, name, block_n, split):
     _schedule(monkeypatch, split)
     prob = _workload(name)

@@ -86,7 +86,7 @@ CASES = [  # (seed, groups, max_m, max_n, max_k, max_l)
 
 @pytest.mark.parametrize("case", CASES, ids=[f"seed{c[0]}-G{c[1]}" for c in CASES])
 @pytest.mark.parametrize("api,block_n,split", [("host", 256, None), ("host", 128, "1"), ("device", 256, "1"),
-                                               ("device", 128, "0")])
+                                               ("device", 128, "0"), ("host", 256, "2"), ("device", 256, "2")])
 def test_random_grouped_calls(nv, oracle_mod, monkeypatch, case, api, block_n, split):
     seed, groups, max_m, max_n, max_k, max_l = case
     if split is not None:
