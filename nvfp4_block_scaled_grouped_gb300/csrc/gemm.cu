@@ -280,7 +280,7 @@ struct Cursor {
     const GemmParams<CAP, DEV> *prm;
     int group_count;
     int tile, tile_end, step;  // whole tiles
-    int w, head_end, w_end;    // split range [w, w_end) of schedule units; head [w, head_end)
+    int w, w_end;              // split range [w, w_end) of schedule units
     int phase;                 // 0: head, 1: whole tiles, 2: rest of the split range
 
     __device__ __forceinline__ void split_segment(Segment &s, const int limit) {
@@ -302,11 +302,16 @@ struct Cursor {
 
     __device__ __forceinline__ bool next(Segment &s) {
         if (phase == 0) {
-            if (w < head_end) {
-                split_segment(s, head_end);
-                return true;
-            }
             phase = 1;
+            if (w < w_end) {
+                // the range's first segment is the head when it is a later
+                // piece of a tile; otherwise it waits for phase 2
+                const int w0 = w;
+                split_segment(s, w_end);
+                if (s.kt0 > 0)
+                    return true;
+                w = w0;
+            }
         }
         if (phase == 1) {
             if (tile < tile_end) {
@@ -703,24 +708,15 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                                        p.ws.partial_slots >= (int)gridDim.x ? p.split : 0);
     const int split = split_tile < total_tiles ? 1 : 0;
     const int P = (split && split_tile == 0 && total_work < (int)gridDim.x) ? total_work : (int)gridDim.x;
-    const int sk0 = tile_first_unit<BN>(p, prefix, wprefix, group_count, split_tile, total_tiles, total_work);
+    const int sk0 = split_tile == 0 ? 0
+                                    : tile_first_unit<BN>(p, prefix, wprefix, group_count, split_tile, total_tiles,
+                                                          total_work);
     // first schedule unit of CTA c's part of the split range
     auto sk_begin = [&](int c) { return sk0 + split_begin(c, P, total_work - sk0); };
-    Cursor<BN, CAP, DEV> cursor0{prefix, wprefix, &p, group_count, (int)blockIdx.x, split_tile, P, 0, 0, 0, 0};
+    Cursor<BN, CAP, DEV> cursor0{prefix, wprefix, &p, group_count, (int)blockIdx.x, split_tile, P, 0, 0, 0};
     if (split && (int)blockIdx.x < P) {
         cursor0.w = sk_begin(blockIdx.x);
         cursor0.w_end = sk_begin(blockIdx.x + 1);
-        cursor0.head_end = cursor0.w;
-        if (cursor0.w < cursor0.w_end) {
-            // the range starts inside a tile: that piece is the head
-            const int g = find_group(wprefix, group_count, cursor0.w);
-            const int wt = group_info<BN>(load_group(p, g)).work_tiles;
-            const int local = cursor0.w - wprefix[g];
-            if (local % wt != 0) {
-                const int tile_end_unit = cursor0.w + (wt - local % wt);
-                cursor0.head_end = tile_end_unit < cursor0.w_end ? tile_end_unit : cursor0.w_end;
-            }
-        }
     }
     if ((int)blockIdx.x >= P)
         cursor0.tile = cursor0.tile_end;  // no whole tiles either
