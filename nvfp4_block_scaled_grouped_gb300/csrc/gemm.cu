@@ -711,10 +711,14 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     const int sk0 = split_tile == 0 ? 0
                                     : tile_first_unit<BN>(p, prefix, wprefix, group_count, split_tile, total_tiles,
                                                           total_work);
+    // The split range goes to the first Psk CTAs, at least one unit each (an
+    // empty part would hold no piece, yet a finishing CTA counts the CTAs
+    // after it whose part starts inside its tile as holding pieces).
+    const int Psk = split ? (total_work - sk0 < P ? total_work - sk0 : P) : 0;
     // first schedule unit of CTA c's part of the split range
-    auto sk_begin = [&](int c) { return sk0 + split_begin(c, P, total_work - sk0); };
+    auto sk_begin = [&](int c) { return sk0 + split_begin(c, Psk, total_work - sk0); };
     Cursor<BN, CAP, DEV> cursor0{prefix, wprefix, &p, group_count, (int)blockIdx.x, split_tile, P, 0, 0, 0};
-    if (split && (int)blockIdx.x < P) {
+    if (split && (int)blockIdx.x < Psk) {
         cursor0.w = sk_begin(blockIdx.x);
         cursor0.w_end = sk_begin(blockIdx.x + 1);
     }
@@ -801,7 +805,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 // reading it have completed, oldest stage first.
                 const int cta = blockIdx.x;
                 int pieces = 0;
-                while (cta + pieces + 1 < P && sk_begin(cta + pieces + 1) < sg.w_tile_end)
+                while (cta + pieces + 1 < Psk && sk_begin(cta + pieces + 1) < sg.w_tile_end)
                     ++pieces;
                 bool flags_ok = true;
                 for (int c2 = cta + 1; c2 <= cta + pieces && flags_ok; ++c2) {

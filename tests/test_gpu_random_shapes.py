@@ -105,3 +105,33 @@ def test_random_grouped_calls(nv, oracle_mod, monkeypatch, case, api, block_n, s
     torch.cuda.synchronize()
     assert nv.device_status() == 0
     _check(oracle_mod, sizes, per_group, dev, f"{api} BN={block_n} split={split} seed={seed}")
+
+
+@pytest.mark.parametrize("extra_tiles", [1, 8])
+@pytest.mark.parametrize("api", ["host", "device"])
+def test_split_remainder_smaller_than_the_grid(nv, oracle_mod, monkeypatch, extra_tiles, api):
+    """Whole waves plus a split remainder (forced) whose schedule units are
+    fewer than the CTAs: the remainder must go to as many CTAs as it has
+    units, each finishing CTA waiting only for CTAs that hold a piece."""
+    monkeypatch.setenv("NVFP4_SPLIT", "2")
+    nv.set_tile_n(256)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    m, n, k = 128 * (sms + extra_tiles), 256, 512          # sms + extra tiles of 2 k-tiles each
+    from nvfp4_block_scaled_grouped_gb300 import workloads
+    from nvfp4_block_scaled_grouped_gb300.device import DeviceProblem
+    prob = workloads.make_problem("tiny", seed=500 + extra_tiles, sizes=[(m, n, k, 1)])
+    dp = DeviceProblem.upload(prob)
+    if api == "host":
+        dp.run()
+    else:
+        t = nv.DeviceGroupTable(1)
+        t.set(dp.problem_sizes, dp.A, dp.B, dp.SFA, dp.SFB, dp.C)
+        t.run()
+    torch.cuda.synchronize()
+    assert nv.device_status() == 0
+    c = dp.c_host()[0]
+    rows = np.concatenate([np.arange(m - 128 * extra_tiles, m), np.random.default_rng(1).integers(0, m, 512)])
+    rows = rows.astype(np.int32)
+    cols = np.random.default_rng(2).integers(0, n, rows.size).astype(np.int32)
+    ref = oracle_mod.gemm_sampled(m, n, k, prob.A[0], prob.B[0], prob.SFA[0], prob.SFB[0], rows, cols)
+    assert_parity(c[rows, cols], ref, f"remainder of {extra_tiles} tiles")
