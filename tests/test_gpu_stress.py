@@ -1,0 +1,82 @@
+"""A compact randomised stress of the cross-CTA protocols (descriptor
+publication, split-tile flags and epochs, the per-call counters): a seeded
+sequence of grouped calls of random shapes, with random schedules and tile
+widths, through the host-table and device-table entry points and replayed CUDA
+graphs, on two streams; every call's status must be clean and its outputs must
+match the oracle on samples."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from parity import parity_mask
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    from nvfp4_block_scaled_grouped_gb300 import build
+    build.build_library()
+    import nvfp4_block_scaled_grouped_gb300 as nv
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.init()
+    return nv
+
+
+def test_random_call_sequence(nv, oracle_mod, monkeypatch):
+    from nvfp4_block_scaled_grouped_gb300 import workloads
+    from nvfp4_block_scaled_grouped_gb300.device import DeviceProblem
+    rng = np.random.default_rng(2024)
+    streams = [torch.cuda.current_stream(), torch.cuda.Stream()]
+    failures = []
+    try:
+        for call in range(120):
+            G = int(rng.choice([1, 2, 3, 8, 20, 70]))
+            sizes = [(0 if rng.random() < 0.1 else int(rng.integers(1, 300)), 32 * int(rng.integers(1, 12)),
+                      32 * int(rng.integers(0, 40)), 1) for _ in range(G)]
+            prob = workloads.make_problem("tiny", seed=int(rng.integers(1 << 30)), sizes=sizes)
+            dp = DeviceProblem.upload(prob)
+            monkeypatch.setenv("NVFP4_SPLIT", str(rng.choice(["0", "1", "2", "-1"])))
+            nv.set_tile_n(int(rng.choice([0, 128, 256])))
+            s = streams[int(rng.integers(0, 2))]
+            mode = str(rng.choice(["host", "device", "graph"]))
+            torch.cuda.synchronize()
+            if mode == "host":
+                dp.run(s)
+            elif mode == "device":
+                t = nv.DeviceGroupTable(G)
+                t.set(dp.problem_sizes, dp.A, dp.B, dp.SFA, dp.SFB, dp.C)
+                torch.cuda.synchronize()
+                t.run(s)
+            else:
+                s = torch.cuda.Stream()
+                dp.run(s)
+                s.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s):
+                    dp.run(s)
+                for c in dp.C:
+                    c.fill_(float("nan"))
+                torch.cuda.synchronize()
+                g.replay()
+                g.replay()
+            torch.cuda.synchronize()
+            st = nv.device_status(s)
+            ok = st == 0
+            for gi, ((m, n, k, _), c) in enumerate(zip(sizes, dp.c_host())):
+                if m == 0 or n == 0:
+                    continue
+                if k == 0:
+                    ok &= bool(np.all(c.view(np.uint16) == 0))
+                    continue
+                rows = rng.integers(0, m, 32).astype(np.int32)
+                cols = rng.integers(0, n, 32).astype(np.int32)
+                ref = oracle_mod.gemm_sampled(m, n, k, prob.A[gi], prob.B[gi], prob.SFA[gi], prob.SFB[gi], rows, cols)
+                ok &= bool(parity_mask(c[rows, cols], ref).all())
+            if not ok:
+                failures.append((call, mode, os.environ.get("NVFP4_SPLIT"), st, sizes))
+    finally:
+        nv.set_tile_n(0)
+    assert not failures, failures[:3]
