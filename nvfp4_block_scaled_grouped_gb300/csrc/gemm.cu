@@ -20,7 +20,8 @@
 //       warp 4    TMA producer: A and B tiles (128-byte swizzle) plus the scale
 //                 runs of each 256-K k-tile (1-D bulk copies: a 128-row x 256-K
 //                 slice of the reordered scale layout is 4 consecutive 512-byte
-//                 atoms) into a multi-stage shared-memory ring;
+//                 atoms) into a multi-stage shared-memory ring; the scale runs
+//                 are issued first and land on their own mbarrier;
 //       warps 6-9 scale writers: each copies the stage's scale atoms into its
 //                 own 32-lane quarter of TMEM with two wide tcgen05.st (the
 //                 layout the block-scaled MMA reads: lane l, column c of a
@@ -91,8 +92,11 @@ struct Cfg {
     static constexpr int kTmemCols = 512;
     static_assert(kSfColBase + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
     static constexpr int kThreads = 320;                           // 10 warps
-    static constexpr int kBarrierBytes = 384;
-    static_assert((3 * kStages + 2 * kAccStages) * 8 <= 176, "barrier area");
+    // barrier area: full / empty / scales-written per stage and the
+    // accumulator barriers from 0, scratch from 176, scales-landed per stage
+    // from 384
+    static constexpr int kBarrierBytes = 448;
+    static_assert((3 * kStages + 2 * kAccStages) * 8 <= 176 && kStages <= 8, "barrier area");
     static constexpr int kEpiStageBytes = 32 * 64;                 // per epilogue warp: 32 rows x 32 fp16
     // A finishing CTA receives the next piece's partial tile in ring stages,
     // kPartialChunksPerStage 16 KiB chunks (32 columns x 128 rows fp32) per
@@ -534,6 +538,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (C::kStages + s); };
     auto sff_bar = [&](int s) { return bars + 8u * (2 * C::kStages + s); };
+    auto sfl_bar = [&](int s) { return bars + 384u + 8u * s; };  // the stage's scale atoms landed
     auto accf_bar = [&](int a) { return bars + 8u * (3 * C::kStages + a); };
     auto acce_bar = [&](int a) { return bars + 8u * (3 * C::kStages + C::kAccStages + a); };
     const uint32_t drain_bar = bars + 176;    // the MMA thread's issued MMAs have completed
@@ -547,7 +552,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     volatile int *s_epi_ok = reinterpret_cast<volatile int *>(bar_area + 208);  // [3]: by segment parity, tail
     volatile uint32_t *s_epoch = reinterpret_cast<volatile uint32_t *>(bar_area + 224);  // this call's epoch
     TailState *s_tail = reinterpret_cast<TailState *>(bar_area + 256);
-    static_assert(256 + sizeof(TailState) <= C::kBarrierBytes, "barrier area");
+    static_assert(256 + sizeof(TailState) <= 384, "barrier area");
     uint8_t *epi_stage = bar_area + C::kBarrierBytes;                // [4 warps][32 rows][64 B]
     int32_t *prefix;
     if constexpr (C::kSmemPrefix)
@@ -563,6 +568,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 ptx::mbar_init(full_bar(s), 1);
                 ptx::mbar_init(empty_bar(s), 1);
                 ptx::mbar_init(sff_bar(s), 4);
+                ptx::mbar_init(sfl_bar(s), 1);
             }
             for (int a = 0; a < C::kAccStages; ++a) {
                 ptx::mbar_init(accf_bar(a), 1);
@@ -778,17 +784,22 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                     const uint32_t sf_bytes = (uint32_t)nkb * kSfAtomBytes;
                     const uint32_t st = smem_base + stage * C::kStageBytes;
                     const uint32_t fb = full_bar(stage);
-                    ptx::mbar_arrive_expect_tx(fb, C::kABytes + C::kBBytes + sf_bytes * (1 + sfb_blocks));
+                    // The scale atoms go first, on their own barrier: they land
+                    // well before the operand tiles, so the scale writers move
+                    // them into TMEM while A and B are still in flight.
+                    const uint32_t sb = sfl_bar(stage);
+                    ptx::mbar_arrive_expect_tx(sb, sf_bytes * (1 + sfb_blocks));
+                    ptx::bulk_load(st + C::kABytes + C::kBBytes, sfa + (size_t)(4 * kt) * kSfAtomBytes, sf_bytes,
+                                   sb, pol_a);
+                    for (int j = 0; j < sfb_blocks; ++j)
+                        ptx::bulk_load(st + C::kABytes + C::kBBytes + C::kSfaBytes + j * 4 * kSfAtomBytes,
+                                       sfb + ((size_t)j * k_blocks + 4 * kt) * kSfAtomBytes, sf_bytes, sb, pol_b);
+                    ptx::mbar_arrive_expect_tx(fb, C::kABytes + C::kBBytes);
                     // batch b's rows start at b * m (b * n) of the group's stack;
                     // rows a tile reads past its batch only reach accumulator
                     // rows / columns that the epilogue does not store
                     ptx::tma_load_2d(st, tmap_a, kt * 128, sg.b * gi.m + sg.tm * kBlockM, fb, pol_a);
                     ptx::tma_load_2d(st + C::kABytes, tmap_b, kt * 128, sg.b * gi.n + sg.tn * BN, fb, pol_b);
-                    ptx::bulk_load(st + C::kABytes + C::kBBytes, sfa + (size_t)(4 * kt) * kSfAtomBytes, sf_bytes,
-                                   fb, pol_a);
-                    for (int j = 0; j < sfb_blocks; ++j)
-                        ptx::bulk_load(st + C::kABytes + C::kBBytes + C::kSfaBytes + j * 4 * kSfAtomBytes,
-                                       sfb + ((size_t)j * k_blocks + 4 * kt) * kSfAtomBytes, sf_bytes, fb, pol_b);
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::kStages) {
@@ -858,6 +869,8 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                     const uint32_t par = (armed_parity >> s) & 1u;
                     const uint64_t t0 = ptx::globaltimer();
                     while (!ptx::mbar_try_wait(full_bar(s), par) && ptx::globaltimer() - t0 < drain_ns) {
+                    }
+                    while (!ptx::mbar_try_wait(sfl_bar(s), par) && ptx::globaltimer() - t0 < drain_ns) {
                     }
                 }
             }
@@ -940,7 +953,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             for (int kt = sg.kt0; kt < kend; ++kt) {
                 int got = 0;
                 if (lane == 0)
-                    got = wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status, kStatusMmaTimeout)
+                    got = wait_bounded(sfl_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status, kStatusMmaTimeout)
                               ? 1
                               : 0;
                 got = __shfl_sync(0xffffffffu, got, 0);
@@ -948,7 +961,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                     ok = false;
                     break;
                 }
-                (void)ptx::mbar_try_wait(full_bar(stage), phase);  // every lane acquires the landed stage
+                (void)ptx::mbar_try_wait(sfl_bar(stage), phase);  // every lane acquires the landed scales
                 const int nkb = (k_blocks - 4 * kt) < 4 ? (k_blocks - 4 * kt) : 4;
                 const uint8_t *st_sfa = smem + stage * C::kStageBytes + C::kABytes + C::kBBytes;
                 const uint8_t *st_sfb = st_sfa + C::kSfaBytes;
