@@ -223,21 +223,21 @@ __device__ __forceinline__ int find_group(const int32_t *prefix, int group_count
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                              uint64_t timeout_ns, uint32_t *status, uint32_t bit) {
-    if (ptx::mbar_try_wait(bar, parity))
+    // Each attempt suspends the thread for at most the bound (capped at
+    // 1 ms), and the bound is checked after every failed one.
+    const uint32_t hint = timeout_ns < 1000000ull ? (uint32_t)timeout_ns : 1000000u;
+    if (ptx::mbar_try_wait_hint(bar, parity, hint))
         return true;
     const uint64_t t0 = ptx::globaltimer();
-    uint32_t spins = 0;
     while (true) {
-        if (ptx::mbar_try_wait(bar, parity))
+        if (ptx::mbar_try_wait_hint(bar, parity, hint))
             return true;
-        if ((++spins & 15u) == 0) {
-            if (*abort_flag)
-                return false;
-            if (ptx::globaltimer() - t0 > timeout_ns) {
-                *abort_flag = 1;
-                atomicOr(status, bit);
-                return false;
-            }
+        if (*abort_flag)
+            return false;
+        if (ptx::globaltimer() - t0 > timeout_ns) {
+            *abort_flag = 1;
+            atomicOr(status, bit);
+            return false;
         }
     }
 }
@@ -622,6 +622,10 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::kTmemCols);
         ptx::tmem_relinquish();
     } else if (warp == 6) {
+        // This call's epoch, for the producer, the partial-tile flags and the
+        // counter reset (read before the producer counts this CTA as done).
+        if (lane == 0)
+            *s_epoch = call_epoch();
         // Exclusive prefix sums of output tiles and schedule units per group.
         if constexpr (DEV) {
             // The caller's table in global memory: 32 groups per step, one per
@@ -740,17 +744,22 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
             int prev_g = -1;
-            const uint32_t epoch = call_epoch();
-            *s_epoch = epoch;
+            const uint32_t epoch = *s_epoch;
             // every group's descriptors are patched by some CTA at start-up
             bool ok = !publish || wait_counter(p.ws.desc_count, gridDim.x, abort_flag, p.timeout_ns, p.ws.status);
             // Once every CTA is past its descriptor wait and has read the
-            // epoch, the last one resets the call counters for the next call.
-            if (atomicAdd(p.ws.done, 1u) == gridDim.x - 1) {
-                *p.ws.desc_count = 0;
-                *p.ws.done = 0;
-                *p.ws.epoch = epoch;
-            }
+            // epoch (set-up, warp 6), the last one resets the call counters
+            // for the next call. Counted after this CTA's first copies are
+            // issued (or when it has none), off the path to its first MMA.
+            bool counted = false;
+            auto count_done = [&]() {
+                counted = true;
+                if (atomicAdd(p.ws.done, 1u) == gridDim.x - 1) {
+                    *p.ws.desc_count = 0;
+                    *p.ws.done = 0;
+                    *p.ws.epoch = *s_epoch;
+                }
+            };
             Cursor<BN, CAP, DEV> cur = cursor0;
             Segment sg;
             bool any = false;
@@ -806,8 +815,12 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                         stage = 0;
                         phase ^= 1u;
                     }
+                    if (!counted)
+                        count_done();
                 }
             }
+            if (!counted)
+                count_done();
             if (ok && any && split && sg.kt0 == 0 && sg.kt1 < sg.ktg && !*abort_flag) {
                 // The last segment is the first piece of a split tile. Once the
                 // later pieces are published (they are their CTAs' first
