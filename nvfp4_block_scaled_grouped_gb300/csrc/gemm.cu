@@ -14,8 +14,9 @@
 //     releases them and adds 1 to a publication counter; producers wait for
 //     all CTAs before their first copy (the per-group descriptor patching of
 //     submission 506336, TMA warp, and the descriptor initialisation kernel of
-//     submission 499344, done inside the one launch). The last producer past
-//     that wait resets the call counters for the next call.
+//     submission 499344, done inside the one launch). Once past that wait
+//     and its first copies, each producer counts its CTA as done; the last
+//     one resets the call counters for the next call.
 // Roles:
 //       warp 4    TMA producer: A and B tiles (128-byte swizzle) plus the scale
 //                 runs of each 256-K k-tile (1-D bulk copies: a 128-row x 256-K
@@ -280,16 +281,18 @@ __device__ __forceinline__ int split_begin(int c, int p, int total_work) {
 // finishes as its last segment).
 template <int BN, int CAP, bool DEV>
 struct Cursor {
+    // (the kernel parameters are passed to next() by reference rather than
+    // kept here: through a stored pointer they would be read with generic
+    // loads instead of from the constant bank, about 1 us per segment)
     const int32_t *prefix, *wprefix;
-    const GemmParams<CAP, DEV> *prm;
     int group_count;
     int tile, tile_end, step;  // whole tiles
     int w, w_end;              // split range [w, w_end) of schedule units
     int phase;                 // 0: head, 1: whole tiles, 2: rest of the split range
 
-    __device__ __forceinline__ void split_segment(Segment &s, const int limit) {
+    __device__ __forceinline__ void split_segment(const GemmParams<CAP, DEV> &p, Segment &s, const int limit) {
         s.g = find_group(wprefix, group_count, w);
-        const GInfo gi = group_info<BN>(load_group(*prm, s.g));
+        const GInfo gi = group_info<BN>(load_group(p, s.g));
         const int local = w - wprefix[s.g];
         const int t = local / gi.work_tiles;
         s.ktg = gi.work_tiles;
@@ -304,14 +307,14 @@ struct Cursor {
         w += s.kt1 - s.kt0;
     }
 
-    __device__ __forceinline__ bool next(Segment &s) {
+    __device__ __forceinline__ bool next(const GemmParams<CAP, DEV> &p, Segment &s) {
         if (phase == 0) {
             phase = 1;
             if (w < w_end) {
                 // the range's first segment is the head when it is a later
                 // piece of a tile; otherwise it waits for phase 2
                 const int w0 = w;
-                split_segment(s, w_end);
+                split_segment(p, s, w_end);
                 if (s.kt0 > 0)
                     return true;
                 w = w0;
@@ -320,7 +323,7 @@ struct Cursor {
         if (phase == 1) {
             if (tile < tile_end) {
                 s.g = find_group(prefix, group_count, tile);
-                const GInfo gi = group_info<BN>(load_group(*prm, s.g));
+                const GInfo gi = group_info<BN>(load_group(p, s.g));
                 const int t = tile - prefix[s.g];
                 s.b = t / gi.tiles_mn;
                 const int tb = t - s.b * gi.tiles_mn;
@@ -336,7 +339,7 @@ struct Cursor {
             phase = 2;
         }
         if (w < w_end) {
-            split_segment(s, w_end);
+            split_segment(p, s, w_end);
             return true;
         }
         return false;
@@ -612,20 +615,23 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         __syncwarp();
         if (publish && lane == 0)
             ptx::red_release_add_gpu(p.ws.desc_count, 1u);
-        // The producer needs the barriers and the prefix sums, not TMEM: it
-        // starts once warp 6 has the prefix sums, while the TMEM allocation
-        // may still be in progress.
+        // The producer needs the barriers, the prefix sums and the epoch, not
+        // TMEM: it starts once warp 6 has the prefix sums and warp 7 the
+        // epoch, while the TMEM allocation may still be in progress.
         __syncwarp();
-        ptx::named_barrier(2, 64);
+        ptx::named_barrier(2, 96);
         ptx::named_barrier_arrive(3, C::kThreads);
     } else if (warp == 5) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::kTmemCols);
         ptx::tmem_relinquish();
-    } else if (warp == 6) {
+    } else if (warp == 7) {
         // This call's epoch, for the producer, the partial-tile flags and the
         // counter reset (read before the producer counts this CTA as done).
         if (lane == 0)
             *s_epoch = call_epoch();
+        __syncwarp();
+        ptx::named_barrier_arrive(2, 96);
+    } else if (warp == 6) {
         // Exclusive prefix sums of output tiles and schedule units per group.
         if constexpr (DEV) {
             // The caller's table in global memory: 32 groups per step, one per
@@ -695,7 +701,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             }
         }
         __syncwarp();
-        ptx::named_barrier_arrive(2, 64);
+        ptx::named_barrier_arrive(2, 96);
     }
     uint32_t tmem_base = 0;  // warp 4 reads it after the role loops
     if (warp != 4) {
@@ -727,7 +733,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     const int Psk = split ? (total_work - sk0 < P ? total_work - sk0 : P) : 0;
     // first schedule unit of CTA c's part of the split range
     auto sk_begin = [&](int c) { return sk0 + split_begin(c, Psk, total_work - sk0); };
-    Cursor<BN, CAP, DEV> cursor0{prefix, wprefix, &p, group_count, (int)blockIdx.x, split_tile, P, 0, 0, 0};
+    Cursor<BN, CAP, DEV> cursor0{prefix, wprefix, group_count, (int)blockIdx.x, split_tile, P, 0, 0, 0};
     if (split && (int)blockIdx.x < Psk) {
         cursor0.w = sk_begin(blockIdx.x);
         cursor0.w_end = sk_begin(blockIdx.x + 1);
@@ -763,7 +769,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             Cursor<BN, CAP, DEV> cur = cursor0;
             Segment sg;
             bool any = false;
-            while (ok && cur.next(sg)) {
+            while (ok && cur.next(p, sg)) {
                 any = true;
                 const GInfo gi = group_info<BN>(load_group(p, sg.g));
                 const int k_tiles = gi.k_tiles;
@@ -896,7 +902,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             bool ok = true;
             Cursor<BN, CAP, DEV> cur = cursor0;
             Segment sg;
-            while (ok && cur.next(sg)) {
+            while (ok && cur.next(p, sg)) {
                 const GInfo gi = group_info<BN>(load_group(p, sg.g));
                 const int k_tiles = gi.k_tiles;
                 const int k_blocks = gi.k_blocks;
@@ -958,7 +964,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         bool ok = true;
         Cursor<BN, CAP, DEV> cur = cursor0;
         Segment sg;
-        while (ok && cur.next(sg)) {
+        while (ok && cur.next(p, sg)) {
             const GInfo gi = group_info<BN>(load_group(p, sg.g));
             const int k_tiles = gi.k_tiles;
             const int k_blocks = gi.k_blocks;
@@ -1031,10 +1037,10 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         bool ok = true;
         Cursor<BN, CAP, DEV> cur = cursor0;
         Segment sg;
-        const bool have = cur.next(sg);
+        const bool have = cur.next(p, sg);
         while (have) {
             Segment nx;
-            if (!cur.next(nx))
+            if (!cur.next(p, nx))
                 break;
             const GInfo gi = group_info<BN>(load_group(p, sg.g));
             // a first piece of a split tile is always a CTA's last segment
