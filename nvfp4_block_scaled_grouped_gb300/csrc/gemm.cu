@@ -615,6 +615,15 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         __syncwarp();
         if (publish && lane == 0)
             ptx::red_release_add_gpu(p.ws.desc_count, 1u);
+        // When no descriptor changes in this call, start fetching those of
+        // the first 16 groups (lane: group lane / 2, A or B) into the
+        // descriptor cache while set-up goes on (non-empty groups only: the
+        // slots of the others may hold anything).
+        if (!publish && lane < 2 * group_count) {
+            const GroupArgs a = load_group(p, lane >> 1);
+            if (a.m > 0 && a.n > 0 && a.k > 0 && a.l > 0)
+                ptx::tmap_prefetch(p.ws.tmaps + (size_t)lane * kDescBytes);
+        }
         // The producer needs the barriers, the prefix sums and the epoch, not
         // TMEM: it starts once warp 6 has the prefix sums and warp 7 the
         // epoch, while the TMEM allocation may still be in progress.

@@ -118,6 +118,11 @@ __device__ __forceinline__ void tmap_acquire(const void *tmap) {
     asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(tmap) : "memory");
 }
 
+// Start fetching a tensor map into the descriptor cache.
+__device__ __forceinline__ void tmap_prefetch(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
 __device__ __forceinline__ void tmap_release() {
     asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
 }
