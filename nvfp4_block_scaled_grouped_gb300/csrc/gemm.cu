@@ -754,7 +754,8 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         // ===================== TMA producer =====================
         if (lane == 0) {
             const uint64_t pol_a = ptx::l2_policy_evict_last();
-            const uint64_t pol_b = ptx::l2_policy_evict_normal();
+            const uint64_t pol_keep = ptx::l2_policy_evict_last();
+            const uint64_t pol_once = ptx::l2_policy_evict_first();
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
@@ -786,6 +787,8 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 if (sg.kt0 >= kend)
                     continue;  // k == 0 tile: nothing to load
                 const int k_blocks = gi.k_blocks;
+                // B panels read by one m-tile stream through L2; the others stay
+                const uint64_t pol_b = gi.tiles_m > 1 ? pol_keep : pol_once;
                 const uint8_t *tmap_a = p.ws.tmaps + (size_t)sg.g * 256;
                 const uint8_t *tmap_b = tmap_a + 128;
                 if (sg.g != prev_g) {
