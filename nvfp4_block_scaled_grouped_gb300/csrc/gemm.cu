@@ -17,12 +17,17 @@
 //     submission 499344, done inside the one launch). Once past that wait
 //     and its first copies, each producer counts its CTA as done; the last
 //     one resets the call counters for the next call.
+// Set-up is split across warps: 4 initialises the barriers and patches
+// descriptors, 5 allocates TMEM, 6 builds the prefix sums, 7 reads the call
+// epoch; the producer starts as soon as 4, 6 and 7 are done.
 // Roles:
 //       warp 4    TMA producer: A and B tiles (128-byte swizzle) plus the scale
 //                 runs of each 256-K k-tile (1-D bulk copies: a 128-row x 256-K
 //                 slice of the reordered scale layout is 4 consecutive 512-byte
 //                 atoms) into a multi-stage shared-memory ring; the scale runs
-//                 are issued first and land on their own mbarrier;
+//                 are issued first and land on their own mbarrier; A panels
+//                 (re-read per n-tile) are kept in L2 with evict-last, B
+//                 panels only when the group has more than one m-tile;
 //       warps 6-9 scale writers: each copies the stage's scale atoms into its
 //                 own 32-lane quarter of TMEM with two wide tcgen05.st (the
 //                 layout the block-scaled MMA reads: lane l, column c of a
