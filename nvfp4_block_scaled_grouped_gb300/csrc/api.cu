@@ -43,6 +43,7 @@ struct DeviceState {
     CUtensorMap tmpl_a;       // box 128 B x 128 rows
     CUtensorMap tmpl_b128;    // box 128 B x 128 rows
     CUtensorMap tmpl_b256;    // box 128 B x 256 rows
+    CUtensorMap tmpl_sfb;     // 8-byte words, box 256 words (4 scale atoms) x 2 rows, no swizzle
 };
 
 constexpr int kMaxDevices = 64;
@@ -73,6 +74,23 @@ int encode_template(EncodeTiledFn encode, CUtensorMap *out, void *addr, uint32_t
     return NVFP4_OK;
 }
 
+// Encode the template of the B-scale map: a 2-D array of 8-byte words, dims
+// {words per 128-row block, row blocks} (patched per group in the kernel), box
+// {256 words = 4 scale atoms, 2 row blocks}, no swizzle. Out-of-bounds words
+// read as zero.
+int encode_sfb_template(EncodeTiledFn encode, CUtensorMap *out, void *addr) {
+    const cuuint64_t dims[2] = {256, 2};
+    const cuuint64_t strides[1] = {2048};
+    const cuuint32_t box[2] = {256, 2};
+    const cuuint32_t elem[2] = {1, 1};
+    CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, addr, dims, strides, box, elem,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled failed for the scale map (CUresult %d)", (int)r);
+    return NVFP4_OK;
+}
+
 // Caller holds g_mutex.
 int device_state(int device, void *any_device_buffer, DeviceState **out) {
     if (device < 0 || device >= kMaxDevices)
@@ -98,6 +116,8 @@ int device_state(int device, void *any_device_buffer, DeviceState **out) {
             s = encode_template(encode, &st.tmpl_b128, any_device_buffer, 128);
         if (s == NVFP4_OK)
             s = encode_template(encode, &st.tmpl_b256, any_device_buffer, 256);
+        if (s == NVFP4_OK)
+            s = encode_sfb_template(encode, &st.tmpl_sfb, any_device_buffer);
         if (s != NVFP4_OK)
             return s;
         e = prepare_gemm_kernels(device);
@@ -285,21 +305,26 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
         // runs whenever it is replayed: it uses region 1 (when the workspace
         // has one, else region 0 with the cache dropped) and patches every
         // slot it uses.
-        if (state->descs.size() < 2 * (size_t)capacity || (graph && regions < 2))
-            state->descs.assign(2 * (size_t)capacity, DescKey());
+        if (state->descs.size() < kDescPerGroup * (size_t)capacity || (graph && regions < 2))
+            state->descs.assign(kDescPerGroup * (size_t)capacity, DescKey());
         desc_maps = 0;
         for (int g = 0; g < group_count; ++g) {
             GroupArgs &a = args[g];
             a.patch = 0;
             if (a.m <= 0 || a.n <= 0 || a.k <= 0)
                 continue;
-            const DescKey ka{a.a, (int32_t)a.l * a.m, a.k, kBlockM}, kb{a.b, (int32_t)a.l * a.n, a.k, block_n};
-            if (graph || !(state->descs[2 * g] == ka)) {
+            const DescKey ka{a.a, (int32_t)a.l * a.m, a.k, kBlockM}, kb{a.b, (int32_t)a.l * a.n, a.k, block_n},
+                ks{a.sfb, (int32_t)a.l * ((a.n + kBlockM - 1) / kBlockM), a.k, 2};
+            if (graph || !(state->descs[kDescPerGroup * g] == ka)) {
                 a.patch |= 1;
                 ++desc_maps;
             }
-            if (graph || !(state->descs[2 * g + 1] == kb)) {
+            if (graph || !(state->descs[kDescPerGroup * g + 1] == kb)) {
                 a.patch |= 2;
+                ++desc_maps;
+            }
+            if (graph || !(state->descs[kDescPerGroup * g + 2] == ks)) {
+                a.patch |= 4;
                 ++desc_maps;
             }
         }
@@ -317,7 +342,7 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
     if (graph && regions > 1)
         ws = second_region(ws);
     const void *tmpl_b = block_n == 256 ? (const void *)&st->tmpl_b256 : (const void *)&st->tmpl_b128;
-    e = launch_grouped(cfg, args, ws, &st->tmpl_a, tmpl_b, stream);
+    e = launch_grouped(cfg, args, ws, &st->tmpl_a, tmpl_b, &st->tmpl_sfb, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "grouped GEMM launch");  // nothing ran, no slot was written
     if (graph)
@@ -325,9 +350,12 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
     for (int g = 0; g < group_count; ++g) {
         const GroupArgs &a = args[g];
         if (a.patch & 1)
-            state->descs[2 * g] = DescKey{a.a, (int32_t)a.l * a.m, a.k, kBlockM};
+            state->descs[kDescPerGroup * g] = DescKey{a.a, (int32_t)a.l * a.m, a.k, kBlockM};
         if (a.patch & 2)
-            state->descs[2 * g + 1] = DescKey{a.b, (int32_t)a.l * a.n, a.k, block_n};
+            state->descs[kDescPerGroup * g + 1] = DescKey{a.b, (int32_t)a.l * a.n, a.k, block_n};
+        if (a.patch & 4)
+            state->descs[kDescPerGroup * g + 2] =
+                DescKey{a.sfb, (int32_t)a.l * ((a.n + kBlockM - 1) / kBlockM), a.k, 2};
     }
     return NVFP4_OK;
 }
@@ -346,7 +374,7 @@ int launch_device_table(int group_count, const DeviceTable &dt, int block_n, voi
     GemmLaunch cfg;
     cfg.block_n = block_n;
     cfg.group_count = group_count;
-    cfg.desc_maps = 2 * group_count;  // every group's slots are rewritten
+    cfg.desc_maps = kDescPerGroup * group_count;  // every group's slots are rewritten
     cfg.total_tiles = 0;              // derived by the kernel
     cfg.total_work = 0;
     cfg.grid = st->sm_count < slots ? st->sm_count : slots;
@@ -359,7 +387,7 @@ int launch_device_table(int group_count, const DeviceTable &dt, int block_n, voi
     (void)state;  // region 0 and its host cache are left alone
     const WorkspaceView ws = second_region(workspace_view(ws_base, capacity, slots, slots, 2));
     const void *tmpl_b = block_n == 256 ? (const void *)&st->tmpl_b256 : (const void *)&st->tmpl_b128;
-    e = launch_grouped(cfg, nullptr, ws, &st->tmpl_a, tmpl_b, stream);
+    e = launch_grouped(cfg, nullptr, ws, &st->tmpl_a, tmpl_b, &st->tmpl_sfb, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "grouped GEMM launch");
     return NVFP4_OK;

@@ -125,6 +125,7 @@ template <int CAP, bool DEV>
 struct GemmParams {
     alignas(64) uint8_t tmpl_a[128];
     alignas(64) uint8_t tmpl_b[128];
+    alignas(64) uint8_t tmpl_sfb[128];
     WorkspaceView ws;
     DeviceTable dt;
     int32_t group_count, block_n, total_tiles, total_work, split, split_tile, desc_maps;
@@ -153,7 +154,7 @@ __device__ __forceinline__ GroupArgs load_group(const GemmParams<CAP, DEV> &p, i
         a.n = sz.y;
         a.k = sz.z;
         a.l = (uint16_t)(sz.w >= 0 && sz.w <= kMaxBatch ? sz.w : 0);
-        a.patch = 3;
+        a.patch = 7;
         a.a = p.dt.a[g];
         a.b = p.dt.b[g];
         a.sfa = p.dt.sfa[g];
@@ -599,17 +600,28 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             if (a.m <= 0 || a.n <= 0 || a.k <= 0 || a.l == 0)
                 continue;
             const uint32_t row_bytes = (uint32_t)(a.k / 2);
-            for (int which = 0; which < 2; ++which) {
+            // SFB as a 2-D array of 8-byte words: one row per 128-row block
+            // of B (all batches stacked), ceil(k / 64) atoms of 512 B per row
+            const uint32_t sf_row_words = (uint32_t)ceil_div_i(a.k, kMmaK) * (kSfAtomBytes / 8);
+            const uint32_t sf_rows = (uint32_t)a.l * (uint32_t)ceil_div_i(a.n, kBlockM);
+            for (int which = 0; which < kDescPerGroup; ++which) {
                 if (!(a.patch & (1 << which)))
                     continue;
-                uint8_t *t = p.ws.tmaps + ((size_t)g * 2 + which) * kDescBytes;
-                const uint4 *src = reinterpret_cast<const uint4 *>(which ? p.tmpl_b : p.tmpl_a);
+                uint8_t *t = p.ws.tmaps + ((size_t)g * kDescPerGroup + which) * kDescBytes;
+                const uint4 *src =
+                    reinterpret_cast<const uint4 *>(which == 0 ? p.tmpl_a : which == 1 ? p.tmpl_b : p.tmpl_sfb);
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
                     reinterpret_cast<uint4 *>(t)[q] = src[q];
-                ptx::tmap_set_address(t, which ? a.b : a.a);
-                ptx::tmap_set_dims(t, row_bytes, (uint32_t)a.l * (uint32_t)(which ? a.n : a.m));
-                ptx::tmap_set_stride1(t, row_bytes);
+                if (which < 2) {
+                    ptx::tmap_set_address(t, which ? a.b : a.a);
+                    ptx::tmap_set_dims(t, row_bytes, (uint32_t)a.l * (uint32_t)(which ? a.n : a.m));
+                    ptx::tmap_set_stride1(t, row_bytes);
+                } else {
+                    ptx::tmap_set_address(t, a.sfb);
+                    ptx::tmap_set_dims(t, sf_row_words, sf_rows);
+                    ptx::tmap_set_stride1(t, (uint64_t)sf_row_words * 8u);
+                }
                 ++patched;
             }
         }
@@ -621,11 +633,11 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         if (publish && lane == 0)
             ptx::red_release_add_gpu(p.ws.desc_count, 1u);
         // When no descriptor changes in this call, start fetching those of
-        // the first 16 groups (lane: group lane / 2, A or B) into the
+        // the first 10 groups (lane: group lane / 3, A, B or SFB) into the
         // descriptor cache while set-up goes on (non-empty groups only: the
         // slots of the others may hold anything).
-        if (!publish && lane < 2 * group_count) {
-            const GroupArgs a = load_group(p, lane >> 1);
+        if (!publish && lane < kDescPerGroup * group_count && lane < 30) {
+            const GroupArgs a = load_group(p, lane / kDescPerGroup);
             if (a.m > 0 && a.n > 0 && a.k > 0 && a.l > 0)
                 ptx::tmap_prefetch(p.ws.tmaps + (size_t)lane * kDescBytes);
         }
@@ -794,11 +806,14 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                 const int k_blocks = gi.k_blocks;
                 // B panels read by one m-tile stream through L2; the others stay
                 const uint64_t pol_b = gi.tiles_m > 1 ? pol_keep : pol_once;
-                const uint8_t *tmap_a = p.ws.tmaps + (size_t)sg.g * 256;
-                const uint8_t *tmap_b = tmap_a + 128;
+                const uint8_t *tmap_a = p.ws.tmaps + (size_t)sg.g * (kDescPerGroup * kDescBytes);
+                const uint8_t *tmap_b = tmap_a + kDescBytes;
+                const uint8_t *tmap_sfb = tmap_b + kDescBytes;
                 if (sg.g != prev_g) {
                     ptx::tmap_acquire(tmap_a);
                     ptx::tmap_acquire(tmap_b);
+                    if constexpr (BN == 256)
+                        ptx::tmap_acquire(tmap_sfb);
                     prev_g = sg.g;
                 }
                 const uint8_t *sfa = gi.sfa + (size_t)sg.b * gi.sfa_batch + (size_t)sg.tm * k_blocks * kSfAtomBytes;
@@ -820,12 +835,26 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
                     // well before the operand tiles, so the scale writers move
                     // them into TMEM while A and B are still in flight.
                     const uint32_t sb = sfl_bar(stage);
-                    ptx::mbar_arrive_expect_tx(sb, sf_bytes * (1 + sfb_blocks));
-                    ptx::bulk_load(st + C::kABytes + C::kBBytes, sfa + (size_t)(4 * kt) * kSfAtomBytes, sf_bytes,
-                                   sb, pol_a);
-                    for (int j = 0; j < sfb_blocks; ++j)
-                        ptx::bulk_load(st + C::kABytes + C::kBBytes + C::kSfaBytes + j * 4 * kSfAtomBytes,
-                                       sfb + ((size_t)j * k_blocks + 4 * kt) * kSfAtomBytes, sf_bytes, sb, pol_b);
+                    if constexpr (BN == 256) {
+                        // both 128-row blocks of SFB in one 2-D copy (4 atoms x
+                        // 2 rows, zero beyond k and n; a last n-tile with one
+                        // row block reads the next rows, which only reach
+                        // accumulator columns >= n): one copy operation fewer
+                        // per stage, which the ring's round trip pays for
+                        ptx::mbar_arrive_expect_tx(sb, sf_bytes + C::kSfbBytes);
+                        ptx::bulk_load(st + C::kABytes + C::kBBytes, sfa + (size_t)(4 * kt) * kSfAtomBytes, sf_bytes,
+                                       sb, pol_a);
+                        ptx::tma_load_2d(st + C::kABytes + C::kBBytes + C::kSfaBytes, tmap_sfb,
+                                         kt * (4 * kSfAtomBytes / 8), sg.b * gi.sf_row_blocks_b + sg.tn * 2, sb,
+                                         pol_b);
+                    } else {
+                        ptx::mbar_arrive_expect_tx(sb, sf_bytes * (1 + sfb_blocks));
+                        ptx::bulk_load(st + C::kABytes + C::kBBytes, sfa + (size_t)(4 * kt) * kSfAtomBytes, sf_bytes,
+                                       sb, pol_a);
+                        for (int j = 0; j < sfb_blocks; ++j)
+                            ptx::bulk_load(st + C::kABytes + C::kBBytes + C::kSfaBytes + j * 4 * kSfAtomBytes,
+                                           sfb + ((size_t)j * k_blocks + 4 * kt) * kSfAtomBytes, sf_bytes, sb, pol_b);
+                    }
                     ptx::mbar_arrive_expect_tx(fb, C::kABytes + C::kBBytes);
                     // batch b's rows start at b * m (b * n) of the group's stack;
                     // rows a tile reads past its batch only reach accumulator
@@ -1171,11 +1200,12 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
 
 template <int BN, int CAP, bool DEV>
 cudaError_t launch_cap(const GemmLaunch &cfg, const GroupArgs *groups, const WorkspaceView &ws,
-                       const void *tmpl_a, const void *tmpl_b, cudaStream_t stream) {
+                       const void *tmpl_a, const void *tmpl_b, const void *tmpl_sfb, cudaStream_t stream) {
     static_assert(sizeof(GemmParams<CAP, DEV>) <= 32000, "kernel parameter limit");
     GemmParams<CAP, DEV> prm;
     std::memcpy(prm.tmpl_a, tmpl_a, 128);
     std::memcpy(prm.tmpl_b, tmpl_b, 128);
+    std::memcpy(prm.tmpl_sfb, tmpl_sfb, 128);
     prm.ws = ws;
     prm.group_count = cfg.group_count;
     prm.block_n = cfg.block_n;
@@ -1230,7 +1260,7 @@ cudaError_t prepare_gemm_kernels(int /*device*/) {
 }
 
 cudaError_t launch_grouped(const GemmLaunch &cfg, const GroupArgs *groups, const WorkspaceView &ws,
-                           const void *tmpl_a, const void *tmpl_b, cudaStream_t stream) {
+                           const void *tmpl_a, const void *tmpl_b, const void *tmpl_sfb, cudaStream_t stream) {
     if (ws.capacity < cfg.group_count || ws.capacity > NVFP4_MAX_GROUPS)
         return cudaErrorInvalidValue;
     if (cfg.split && ws.partial_slots < cfg.grid)
@@ -1241,19 +1271,19 @@ cudaError_t launch_grouped(const GemmLaunch &cfg, const GroupArgs *groups, const
     if (cfg.device_table) {
         // shared-memory prefix sums up to kMediumGroups groups
         if (cfg.group_count <= kMediumGroups)
-            return wide ? launch_cap<256, kMediumGroups, true>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
-                        : launch_cap<128, kMediumGroups, true>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
-        return wide ? launch_cap<256, NVFP4_MAX_GROUPS, true>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
-                    : launch_cap<128, NVFP4_MAX_GROUPS, true>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
+            return wide ? launch_cap<256, kMediumGroups, true>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream)
+                        : launch_cap<128, kMediumGroups, true>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream);
+        return wide ? launch_cap<256, NVFP4_MAX_GROUPS, true>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream)
+                    : launch_cap<128, NVFP4_MAX_GROUPS, true>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream);
     }
     if (cfg.group_count <= kSmallGroups)
-        return wide ? launch_cap<256, kSmallGroups, false>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
-                    : launch_cap<128, kSmallGroups, false>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
+        return wide ? launch_cap<256, kSmallGroups, false>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream)
+                    : launch_cap<128, kSmallGroups, false>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream);
     if (cfg.group_count <= kMediumGroups)
-        return wide ? launch_cap<256, kMediumGroups, false>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
-                    : launch_cap<128, kMediumGroups, false>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
-    return wide ? launch_cap<256, NVFP4_MAX_GROUPS, false>(cfg, groups, ws, tmpl_a, tmpl_b, stream)
-                : launch_cap<128, NVFP4_MAX_GROUPS, false>(cfg, groups, ws, tmpl_a, tmpl_b, stream);
+        return wide ? launch_cap<256, kMediumGroups, false>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream)
+                    : launch_cap<128, kMediumGroups, false>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream);
+    return wide ? launch_cap<256, NVFP4_MAX_GROUPS, false>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream)
+                : launch_cap<128, NVFP4_MAX_GROUPS, false>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream);
 }
 
 }  // namespace nvfp4

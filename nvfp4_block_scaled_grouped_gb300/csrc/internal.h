@@ -24,7 +24,8 @@ constexpr int kSfAtomBytes = 512;  // 128 rows x 4 scale blocks
 // l is the group's batch count: batch b of A starts l-major at row b*m of a
 // [l*m][k/2] stack (likewise B, C and the per-batch scale-atom blocks).
 // `patch` tells the kernel which of the group's descriptors (bit 0: A, bit 1:
-// B) must be rewritten; the others already hold this group's pointer and shape.
+// B, bit 2: SFB) must be rewritten; the others already hold this group's
+// pointer and shape.
 struct GroupArgs {
     int32_t m, n, k;
     uint16_t l, patch;
@@ -54,6 +55,8 @@ __host__ __device__ constexpr size_t round_up(size_t x, size_t a) { return (x + 
 
 constexpr size_t kPartialSlotBytes = sizeof(float) * 128 * 256;
 constexpr int kDescBytes = 128;
+// Descriptor slots per group: A, B and the B scales (SFB).
+constexpr int kDescPerGroup = 3;
 
 // Per-CTA prefix-sum scratch in global memory, used when the group count is
 // too large for the kernel's spare shared memory: [tiles prefix | units prefix].
@@ -69,7 +72,7 @@ __host__ __device__ constexpr size_t cta_prefix_bytes(int capacity) { return 2 *
 //               The last CTA to get there resets both counters and advances
 //               the epoch, so nothing on the host tracks them (calls replayed
 //               from a CUDA graph included).
-//   tmaps       TMA descriptors [regions][capacity][A, B], 128 B each. Region
+//   tmaps       TMA descriptors [regions][capacity][A, B, SFB], 128 B each. Region
 //               0 serves eager host-table calls (its contents are cached on
 //               the host); region 1, where present, serves calls whose
 //               launch may run at another time or patches slots the host
@@ -94,7 +97,7 @@ struct WorkspaceView {
 };
 
 constexpr size_t workspace_bytes(int capacity, int prefix_slots = 0, int partial_slots = 0, int regions = 1) {
-    return 128 + (size_t)kDescBytes * 2 * (size_t)capacity * (size_t)regions +
+    return 128 + (size_t)kDescBytes * kDescPerGroup * (size_t)capacity * (size_t)regions +
            (capacity > kMediumGroups ? cta_prefix_bytes(capacity) * (size_t)prefix_slots : 0) +
            (partial_slots > 0 ? round_up(sizeof(uint32_t) * (size_t)partial_slots, 128) +
                                     kPartialSlotBytes * (size_t)partial_slots
@@ -111,7 +114,7 @@ inline WorkspaceView workspace_view(void *base, int capacity, int prefix_slots =
     v.epoch = reinterpret_cast<uint32_t *>(p + 100);
     p += 128;
     v.tmaps = p;
-    p += (size_t)kDescBytes * 2 * (size_t)capacity * (size_t)regions;
+    p += (size_t)kDescBytes * kDescPerGroup * (size_t)capacity * (size_t)regions;
     v.cta_prefix = nullptr;
     v.prefix_slots = 0;
     if (capacity > kMediumGroups) {
@@ -134,7 +137,7 @@ inline WorkspaceView workspace_view(void *base, int capacity, int prefix_slots =
 
 // The same workspace with descriptor region 1 in place of region 0.
 inline WorkspaceView second_region(WorkspaceView v) {
-    v.tmaps += (size_t)kDescBytes * 2 * (size_t)v.capacity;
+    v.tmaps += (size_t)kDescBytes * kDescPerGroup * (size_t)v.capacity;
     return v;
 }
 
@@ -190,10 +193,10 @@ struct GemmLaunch {
     DeviceTable dt;
 };
 
-// Host launcher (gemm.cu). `tmpl_a` / `tmpl_b` are 128-byte encoded TMA
-// descriptors the kernel patches per group.
+// Host launcher (gemm.cu). `tmpl_a` / `tmpl_b` / `tmpl_sfb` are 128-byte
+// encoded TMA descriptors the kernel patches per group.
 cudaError_t launch_grouped(const GemmLaunch &cfg, const GroupArgs *groups, const WorkspaceView &ws,
-                           const void *tmpl_a, const void *tmpl_b, cudaStream_t stream);
+                           const void *tmpl_a, const void *tmpl_b, const void *tmpl_sfb, cudaStream_t stream);
 cudaError_t prepare_gemm_kernels(int device);
 
 // Host layer (api.cu), shared by the entry points.
