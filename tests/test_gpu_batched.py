@@ -124,3 +124,42 @@ def test_several_problems_in_one_launch(nv, oracle_mod, monkeypatch, split):
         for p, dp in enumerate(dps):
             for g, (c, t) in enumerate(zip(dp.c_host(), together[p])):
                 np.testing.assert_array_equal(c.view(np.uint16), t.view(np.uint16), err_msg=f"problem {p} group {g}")
+
+
+def test_scale_descriptor_follows_batch_layout_over_the_same_buffers(nv, oracle_mod):
+    """The same B and SFB buffers read first as one batch of n = 256 rows and
+    then as l = 4 batches of n = 64 (the same l*n, but 4 instead of 2 blocks of
+    128 scale rows): the cached SFB descriptor must be patched again."""
+    from nvfp4_block_scaled_grouped_gb300 import workloads
+    k, m = 256, 64
+    one = workloads.make_problem("tiny", seed=77, sizes=[(m, 256, k, 1)])
+    B = torch.from_numpy(np.ascontiguousarray(one.B[0])).cuda()
+    sf_rows = one.SFB[0]                                       # [256][k/16] row-major
+    sfb = torch.zeros(4 * nv.scale_bytes(64, k), dtype=torch.uint8, device="cuda")
+    packed1 = nv.pack_scales_tensor(torch.from_numpy(np.ascontiguousarray(sf_rows)).cuda(), k)
+    sfb[: packed1.numel()].copy_(packed1)
+    A1 = torch.from_numpy(np.ascontiguousarray(one.A[0])).cuda()
+    SFA1 = nv.pack_scales_tensor(torch.from_numpy(np.ascontiguousarray(one.SFA[0])).cuda(), k)
+    C1 = torch.full((m, 256), float("nan"), dtype=torch.float16, device="cuda")
+    nv.grouped_gemm_tensors([(m, 256, k, 1)], [A1], [B], [SFA1], [sfb], [C1])
+    torch.cuda.synchronize()
+    assert nv.device_status() == 0
+    ref1 = oracle_mod.grouped_gemm(one.problem_sizes, one.A, one.B, one.SFA, one.SFB)[0]
+    assert_parity(C1.cpu().numpy(), ref1, "n = 256, l = 1")
+
+    # the same buffers as 4 batches of 64 rows of B (batch b: rows 64b .. 64b+63)
+    sfb.copy_(torch.cat([nv.pack_scales_tensor(torch.from_numpy(np.ascontiguousarray(sf_rows[64 * b: 64 * b + 64]))
+                                               .cuda(), k) for b in range(4)]))
+    batches = [workloads.make_problem("tiny", seed=80 + b, sizes=[(m, 64, k, 1)]) for b in range(4)]
+    A4 = torch.from_numpy(np.ascontiguousarray(np.concatenate([p.A[0] for p in batches]))).cuda()
+    SFA4 = torch.cat([nv.pack_scales_tensor(torch.from_numpy(np.ascontiguousarray(p.SFA[0])).cuda(), k)
+                      for p in batches])
+    C4 = torch.full((4 * m, 64), float("nan"), dtype=torch.float16, device="cuda")
+    nv.grouped_gemm_tensors([(m, 64, k, 4)], [A4], [B], [SFA4], [sfb], [C4])
+    torch.cuda.synchronize()
+    assert nv.device_status() == 0
+    c4 = C4.cpu().numpy().reshape(4, m, 64)
+    for b, p in enumerate(batches):
+        ref = oracle_mod.grouped_gemm([(m, 64, k, 1)], p.A, [one.B[0][64 * b: 64 * b + 64]], p.SFA,
+                                      [sf_rows[64 * b: 64 * b + 64]])[0]
+        assert_parity(c4[b], ref, f"l = 4 batch {b}")
