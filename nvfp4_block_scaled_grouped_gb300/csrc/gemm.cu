@@ -1,7 +1,7 @@
 // gemm.cu -- the grouped NVFP4 block-scaled GEMM for sm_103a.
 //
 // One persistent kernel per call, grouped_gemm_kernel<BN, CAP, DEV> (one CTA
-// per SM, 320 threads, cooperative launch so every CTA is resident). The group
+// per SM, 448 threads, cooperative launch so every CTA is resident). The group
 // table (sizes, batch counts and pointers of up to CAP groups) arrives as a
 // __grid_constant__ kernel parameter, or (DEV) stays in the caller's device
 // arrays and is read, and checked, by the kernel. At start-up every CTA
@@ -37,11 +37,15 @@
 //                 (scale_vec::4X = one e4m3 scale per 16 elements),
 //                 128 x BN x 64, four per k-tile, into a TMEM accumulator;
 //                 commits free the smem stage and publish the accumulator;
-//       warps 0-3 epilogue of every segment but the CTA's last: tcgen05.ld of
-//                 the accumulator lanes they own, fp32 -> fp16
-//                 round-to-nearest-even, staged through a swizzled per-warp
-//                 buffer so each store writes 8 rows x 64 B; rows >= m and
-//                 column chunks >= n skipped;
+//       warps 0-3 and 10-13: epilogue of every segment but the CTA's last
+//                 (two warps per TMEM lane quarter, each half of the column
+//                 chunks): tcgen05.ld of the accumulator lanes they own,
+//                 fp32 -> fp16 round-to-nearest-even; a whole tile is moved
+//                 into registers first and the accumulator released to the
+//                 next tile's MMAs before the stores (warps 0-3 stage theirs
+//                 through a swizzled per-warp buffer so each store writes 8
+//                 rows x 64 B, warps 10-13 store each row's 64 B from
+//                 registers); rows >= m and column chunks >= n skipped;
 //       warps 0-7 epilogue of the CTA's last segment, once every role has
 //                 left its loop (the last epilogue is on the critical path).
 //
@@ -97,7 +101,9 @@ struct Cfg {
     static constexpr int kSfColBase = kAccStages * kAccCols;
     static constexpr int kTmemCols = 512;
     static_assert(kSfColBase + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
-    static constexpr int kThreads = 320;                           // 10 warps
+    // 14 warps: 0-3 and 10-13 epilogue, 4 producer, 5 MMA, 6-9 scale writers
+    static constexpr int kThreads = 448;
+    static constexpr int kMaxLoopChunks = BN / 64;  // column chunks per epilogue warp in the loop
     // barrier area: full / empty / scales-written per stage and the
     // accumulator barriers from 0, scratch from 176, scales-landed per stage
     // from 384
@@ -393,15 +399,27 @@ __device__ __forceinline__ int tile_chunks(const GInfo &gi, const Segment &sg) {
 // +31 (tile rows), column chunks [c0, c1). TMEM loads run half a chunk (16
 // columns) ahead of the arithmetic and stores. `buf` is the warp's 2 KiB
 // staging buffer; `smem` the CTA's ring (holding the next piece's partial tile
-// from stage part_stage0 when finishing a split tile).
+// from stage part_stage0 when finishing a split tile). With `release_bar` (a
+// whole tile in the main loop, at most kMaxLoopChunks chunks per warp) the
+// warp first moves its chunks from TMEM into registers and arrives on
+// release_bar, so the next tile's MMAs may start, and then stores them; a
+// null `buf` stores each row's 64 bytes straight from registers.
 template <int BN, int CAP, bool DEV>
 __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, const Segment &sg, const GInfo &gi,
                                               const int kind, const int quarter, const int lane,
                                               const uint32_t t_acc, const int c0, const int c1, uint8_t *buf,
-                                              const uint8_t *smem, const int part_stage0, const int pieces) {
+                                              const uint8_t *smem, const int part_stage0, const int pieces,
+                                              const uint32_t release_bar = 0) {
     using C = Cfg<BN, CAP>;
-    if (c0 >= c1)
+    if (c0 >= c1) {
+        // no chunks for this warp (a narrow tile), but its release still counts
+        if (release_bar != 0) {
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(release_bar);
+        }
         return;
+    }
     const int m = gi.m, n = gi.n;
     const int cta = blockIdx.x;
     const int r_local = quarter * 32 + lane;
@@ -430,6 +448,15 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, con
                 *reinterpret_cast<uint4 *>(c_base + (size_t)grow * (size_t)n + col + 8 * piece) = val;
         }
         __syncwarp();
+    };
+    // without a staging buffer: each lane writes its row's 64 bytes
+    auto store_direct = [&](const int cc, const uint32_t (&h)[16]) {
+        if (row < m) {
+            uint4 *dst = reinterpret_cast<uint4 *>(c_base + (size_t)row * (size_t)n + sg.tn * BN + cc * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                dst[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+        }
     };
     auto pack = [](float x0, float x1) {
         __half2 h2 = __floats2half2_rn(x0, x1);
@@ -503,6 +530,39 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, con
             add_half(vb, cc, 4, h + 8);
             store_chunk(cc, h);
         }
+    } else if (release_bar != 0) {
+        const bool zero = gi.k == 0;
+        uint32_t hs[C::kMaxLoopChunks][16];
+#pragma unroll
+        for (int i = 0; i < C::kMaxLoopChunks; ++i) {
+            const int cc = c0 + i;
+            if (cc < c1) {
+                ptx::tmem_ld_wait();
+                ptx::tmem_ld_32x32b_x16(t_row + cc * 32 + 16, vb);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    hs[i][q] = zero ? 0u : pack(__uint_as_float(va[2 * q]), __uint_as_float(va[2 * q + 1]));
+                ptx::tmem_ld_wait();
+                if (cc + 1 < c1)
+                    ptx::tmem_ld_32x32b_x16(t_row + (cc + 1) * 32, va);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    hs[i][8 + q] = zero ? 0u : pack(__uint_as_float(vb[2 * q]), __uint_as_float(vb[2 * q + 1]));
+            }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            ptx::mbar_arrive(release_bar);
+#pragma unroll
+        for (int i = 0; i < C::kMaxLoopChunks; ++i) {
+            if (c0 + i < c1) {
+                if (buf)
+                    store_chunk(c0 + i, hs[i]);
+                else
+                    store_direct(c0 + i, hs[i]);
+            }
+        }
     } else {
         const bool zero = gi.k == 0;
         uint32_t h[16];
@@ -525,7 +585,7 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, con
 }
 
 template <int BN, int CAP, bool DEV>
-__global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams<CAP, DEV> p) {
+__global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams<CAP, DEV> p) {
     using C = Cfg<BN, CAP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -581,7 +641,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             }
             for (int a = 0; a < C::kAccStages; ++a) {
                 ptx::mbar_init(accf_bar(a), 1);
-                ptx::mbar_init(acce_bar(a), 4);
+                ptx::mbar_init(acce_bar(a), 8);
             }
             ptx::mbar_init(partial_bar, 1);
             ptx::mbar_init(drain_bar, 1);
@@ -1000,7 +1060,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             while (!ptx::mbar_try_wait(drain_bar, 0) && ptx::globaltimer() - t0 < drain_ns) {
             }
         }
-    } else if (warp >= 6) {
+    } else if (warp >= 6 && warp < 10) {
         // ===================== scale writers (warps 6..9) =====================
         // Warp w owns TMEM lanes 32*(w % 4) .. +31 and writes the scale atoms
         // of every stage into that quarter.
@@ -1074,10 +1134,15 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             }
         }
     } else {
-        // ===================== epilogue (warps 0..3) =====================
+        // ================= epilogue (warps 0..3 and 10..13) =================
         // Every segment but the CTA's last; the last is finished below, once
-        // every role has left its loop, with warps 4..7 helping.
+        // every role has left its loop, by warps 0..7. Warp w takes TMEM lane
+        // quarter w % 4; warps 0..3 the first half of the column chunks
+        // (storing through their staging buffers), warps 10..13 the second
+        // (storing straight from registers).
         const int cta = blockIdx.x;
+        const bool first_half = warp < 4;
+        const int quarter = warp & 3;
         int acc = 0, it = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
@@ -1091,28 +1156,36 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
             const GInfo gi = group_info<BN>(load_group(p, sg.g));
             // a first piece of a split tile is always a CTA's last segment
             const int kind = sg.kt0 > 0 ? kEpiCont : kEpiWhole;
-            // One thread waits for the accumulator; the four warps leave or
+            // One thread waits for the accumulator; the eight warps leave or
             // stay together (the TMEM loads are warp-collective).
             if (threadIdx.x == 0)
                 s_epi_ok[it & 1] = wait_bounded(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns, p.ws.status,
                                                 kStatusEpilogueTimeout)
                                        ? 1
                                        : 0;
-            ptx::named_barrier(1, 128);
+            ptx::named_barrier(4, 256);
             if (!s_epi_ok[it & 1]) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-            epilogue_warp<BN, CAP, DEV>(p, sg, gi, kind, warp, lane, tmem_base + (uint32_t)(acc * C::kAccCols), 0,
-                                   tile_chunks<BN>(gi, sg), epi_stage + warp * C::kEpiStageBytes, smem, 0, 0);
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                ptx::mbar_arrive(acce_bar(acc));
+            const int nch = tile_chunks<BN>(gi, sg);
+            const int half = (nch + 1) / 2;
+            // a whole tile releases the accumulator once its chunks are in
+            // registers; a partial tile (fp32) goes out chunk by chunk first
+            const uint32_t t_acc = tmem_base + (uint32_t)(acc * C::kAccCols);
+            epilogue_warp<BN, CAP, DEV>(p, sg, gi, kind, quarter, lane, t_acc, first_half ? 0 : half,
+                                   first_half ? half : nch, first_half ? epi_stage + warp * C::kEpiStageBytes : nullptr,
+                                   smem, 0, 0, kind == kEpiWhole ? acce_bar(acc) : 0u);
+            if (kind != kEpiWhole) {
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(acce_bar(acc));
+            }
             if (kind == kEpiCont) {
                 // publish this CTA's partial tile
-                ptx::named_barrier(1, 128);
+                ptx::named_barrier(4, 256);
                 if (threadIdx.x == 0) {
                     __threadfence();
                     ptx::st_release_gpu(p.ws.flags + cta, *s_epoch);
