@@ -966,19 +966,20 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                     const char *src =
                         reinterpret_cast<const char *>(p.ws.partials) + (size_t)(cta + 1) * kPartialSlotBytes;
                     bool good = true;
-                    for (int cc = 0; cc < nch; ++cc) {
+                    // one copy per ring stage: the chunks of a stage are
+                    // contiguous in the workspace slot and in the stage
+                    for (int cc = 0; cc < nch; cc += C::kPartialChunksPerStage) {
                         const int s = (stage + cc / C::kPartialChunksPerStage) % C::kStages;
-                        if (cc % C::kPartialChunksPerStage == 0 && ((armed >> s) & 1u) &&
+                        if (((armed >> s) & 1u) &&
                             !wait_bounded(empty_bar(s), (armed_parity >> s) & 1u, abort_flag, p.timeout_ns,
                                           p.ws.status, kStatusProducerTimeout)) {
                             good = false;
                             break;
                         }
-                        ptx::mbar_expect_tx(partial_bar, kPartialChunkBytes);
-                        ptx::bulk_load(smem_base + s * C::kStageBytes + (cc % C::kPartialChunksPerStage) *
-                                                                            kPartialChunkBytes,
-                                       src + (size_t)cc * kPartialChunkBytes, kPartialChunkBytes, partial_bar,
-                                       ptx::l2_policy_evict_first());
+                        const int nc = (nch - cc) < C::kPartialChunksPerStage ? (nch - cc) : C::kPartialChunksPerStage;
+                        ptx::mbar_expect_tx(partial_bar, (uint32_t)nc * kPartialChunkBytes);
+                        ptx::bulk_load(smem_base + s * C::kStageBytes, src + (size_t)cc * kPartialChunkBytes,
+                                       (uint32_t)nc * kPartialChunkBytes, partial_bar, ptx::l2_policy_evict_first());
                     }
                     ptx::mbar_arrive(partial_bar);
                     s_tail->part_stage0 = stage;
