@@ -168,7 +168,7 @@ int nvfp4_grouped_gemm_device(int group_count, const nvfp4_problem_size *problem
  *  - at most NVFP4_NOALLOC_MAX_GROUPS (64) groups; more is rejected with
  *    NVFP4_ERR_INVALID_ARG before anything is enqueued;
  *  - the scratch (tile prefix sum, group table, TMA descriptors, status word;
- *    about 21 KiB) is one fixed array in the library's device memory, which
+ *    about 24 KiB) is one fixed array in the library's device memory, which
  *    every GPU that loads the library holds until the process exits. The call
  *    never calls cudaMalloc, cudaFree or any other allocating routine;
  *  - every call on a device shares that array and it keeps the previous
