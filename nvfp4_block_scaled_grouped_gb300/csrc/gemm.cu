@@ -137,12 +137,6 @@ struct GemmParams {
     int32_t group_count, block_n, total_tiles, total_work, split, split_tile, desc_maps;
     uint64_t timeout_ns;
     GroupArgs groups[DEV ? 1 : CAP];
-    // host tables of up to kMediumGroups groups: the exclusive prefix sums of
-    // output tiles and schedule units, computed by the host (the kernel only
-    // copies them into shared memory)
-    static constexpr bool kHostPrefix = !DEV && CAP <= kMediumGroups;
-    int32_t hprefix[kHostPrefix ? CAP + 1 : 1];
-    int32_t hwprefix[kHostPrefix ? CAP + 1 : 1];
 };
 
 __device__ __forceinline__ bool aligned16(const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
@@ -770,13 +764,6 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             if (__any_sync(full, bad) && blockIdx.x == 0 && lane == 0)
                 atomicOr(p.ws.status, kStatusBadGroup);
         } else {
-          if constexpr (GemmParams<CAP, DEV>::kHostPrefix) {
-            // computed by the host: one parallel copy
-            for (int g = lane; g <= group_count; g += 32) {
-                prefix[g] = p.hprefix[g];
-                wprefix[g] = p.hwprefix[g];
-            }
-          } else {
             // The group table lives in the constant bank, where a warp
             // reading different addresses is serialised, so every lane walks
             // all groups with the same index (broadcast reads) and lane g % 32
@@ -798,7 +785,6 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                 prefix[group_count] = bt;
                 wprefix[group_count] = bw;
             }
-          }
         }
         __syncwarp();
         ptx::named_barrier_arrive(2, 96);
@@ -1309,23 +1295,6 @@ cudaError_t launch_cap(const GemmLaunch &cfg, const GroupArgs *groups, const Wor
     } else {
         prm.dt = DeviceTable{};
         std::memcpy(prm.groups, groups, sizeof(GroupArgs) * (size_t)cfg.group_count);
-        if constexpr (GemmParams<CAP, DEV>::kHostPrefix) {
-            // the same sums the kernel would build (tile and schedule-unit
-            // counts per group, exclusive prefix)
-            int32_t bt = 0, bw = 0;
-            for (int g = 0; g < cfg.group_count; ++g) {
-                const GroupArgs &a = groups[g];
-                const int32_t tiles =
-                    (a.m > 0 && a.n > 0) ? ((a.m + kBlockM - 1) / kBlockM) * ((a.n + BN - 1) / BN) * (int32_t)a.l : 0;
-                const int32_t kt = (a.k + kBlockK - 1) / kBlockK;
-                prm.hprefix[g] = bt;
-                prm.hwprefix[g] = bw;
-                bt += tiles;
-                bw += tiles * (kt > 1 ? kt : 1);
-            }
-            prm.hprefix[cfg.group_count] = bt;
-            prm.hwprefix[cfg.group_count] = bw;
-        }
         if (cfg.group_count < CAP)
             std::memset(prm.groups + cfg.group_count, 0, sizeof(GroupArgs) * (size_t)(CAP - cfg.group_count));
     }
