@@ -306,21 +306,21 @@ def gpu_arm(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     dps = [DeviceProblem.upload(p, device=dev) for p in probs]   # uploads, then packs scales (library kernel)
     # The scale-layout pre-pass alone: the row-major scales of every operand
-    # are resident, a spin keeps the GPU busy while the host queues the pack
-    # launches, and events bracket only those launches.
+    # are resident, a spin keeps the GPU busy while the host queues the
+    # launch, and events bracket only the one batched pack launch.
     sf_rows = [(torch.from_numpy(np.ascontiguousarray(sf)).to(dev), k)
                for p in probs for (m, n, k, _), sfa, sfb in zip(p.problem_sizes, p.SFA, p.SFB)
                for sf, rows in ((sfa, m), (sfb, n)) if rows > 0 and k > 0]
+    nv.pack_scales_tensors(sf_rows)   # warm-up: its outputs' memory is then cached for the timed call
     torch.cuda.synchronize()
     t_pack0 = torch.cuda.Event(enable_timing=True)
     t_pack1 = torch.cuda.Event(enable_timing=True)
     torch.cuda._sleep(2_000_000)
     t_pack0.record(stream)
-    for sf, k in sf_rows:
-        nv.pack_scales_tensor(sf, k)
+    packed = nv.pack_scales_tensors(sf_rows)
     t_pack1.record(stream)
     torch.cuda.synchronize()
-    del sf_rows
+    del sf_rows, packed
     dp = DeviceProblem(problem_sizes=[s for d in dps for s in d.problem_sizes], A=[t for d in dps for t in d.A],
                        B=[t for d in dps for t in d.B], SFA=[t for d in dps for t in d.SFA],
                        SFB=[t for d in dps for t in d.SFB], C=[t for d in dps for t in d.C])

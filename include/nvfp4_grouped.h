@@ -58,6 +58,9 @@ typedef enum nvfp4_status {
 
 /* Largest group_count accepted by nvfp4_grouped_gemm. */
 #define NVFP4_MAX_GROUPS 512
+/* Most matrices one nvfp4_pack_scales_batched call packs (the SFA and SFB of
+ * a call with NVFP4_MAX_GROUPS groups). */
+#define NVFP4_PACK_MAX_BATCH 1024
 
 /*
  * nvfp4_grouped_gemm -- the grouped block-scaled GEMM.
@@ -210,6 +213,24 @@ size_t nvfp4_scale_bytes(int rows, int k);
  */
 int nvfp4_pack_scales(const void *sf_rowmajor, int rows, int k, void *sf_atoms,
                       nvfp4_stream_t stream);
+
+/*
+ * nvfp4_pack_scales_batched -- nvfp4_pack_scales for `count` matrices in one
+ * kernel launch (e.g. the SFA and SFB of every group of a call), each matrix
+ * packed exactly as nvfp4_pack_scales packs it.
+ *   count        0 <= count <= NVFP4_PACK_MAX_BATCH.
+ *   sf_rowmajor, rows, k, sf_atoms: HOST arrays of count entries; the
+ *                pointers are DEVICE addresses with the layouts and sizes of
+ *                nvfp4_pack_scales; entries with rows == 0 or k == 0 are
+ *                skipped. No two entries may write overlapping bytes.
+ * Every entry is checked before anything is enqueued: the first bad one
+ * gives NVFP4_ERR_INVALID_ARG (count out of range, null arrays, negative
+ * rows or k, null pointers), NVFP4_ERR_UNSUPPORTED (k % 16 != 0) or
+ * NVFP4_ERR_MISALIGNED (sf_atoms not 16-byte aligned). NVFP4_ERR_CUDA if the
+ * launch fails. Asynchronous on `stream`.
+ */
+int nvfp4_pack_scales_batched(int count, const void *const *sf_rowmajor, const int *rows, const int *k,
+                              void *const *sf_atoms, nvfp4_stream_t stream);
 
 /* Element types of nvfp4_quantize_pack's input. */
 #define NVFP4_DTYPE_BF16 0

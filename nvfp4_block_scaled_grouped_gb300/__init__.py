@@ -28,12 +28,14 @@ __all__ = [
     "Nvfp4Error", "lib", "library_path", "grouped_gemm", "grouped_gemm_tensors", "grouped_gemm_batched",
     "grouped_gemm_device",
     "DeviceGroupTable", "quantize_pack", "quantize_pack_tensor", "DTYPE_BF16", "DTYPE_F16", "pack_scales",
-    "pack_scales_tensor", "scale_bytes", "device_status", "set_tile_n", "MAX_GROUPS", "STATUS",
+    "pack_scales_tensor", "pack_scales_batched", "pack_scales_tensors", "scale_bytes", "device_status",
+    "set_tile_n", "MAX_GROUPS", "PACK_MAX_BATCH", "STATUS",
 ]
 
 _PKG = Path(__file__).resolve().parent
 _LIB_PATH = _PKG / "_lib" / "libnvfp4_grouped.so"
 MAX_GROUPS = 512
+PACK_MAX_BATCH = 1024
 STATUS = {0: "NVFP4_OK", -1: "NVFP4_ERR_INVALID_ARG", -2: "NVFP4_ERR_UNSUPPORTED",
           -3: "NVFP4_ERR_MISALIGNED", -4: "NVFP4_ERR_CUDA", -5: "NVFP4_ERR_TIMEOUT"}
 
@@ -80,6 +82,9 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_scale_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
         L.nvfp4_pack_scales.restype = ctypes.c_int
         L.nvfp4_pack_scales.argtypes = [vp, ctypes.c_int, ctypes.c_int, vp, vp]
+        L.nvfp4_pack_scales_batched.restype = ctypes.c_int
+        L.nvfp4_pack_scales_batched.argtypes = [ctypes.c_int, vpp, ctypes.POINTER(ctypes.c_int),
+                                                ctypes.POINTER(ctypes.c_int), vpp, vp]
         L.nvfp4_device_status.restype = ctypes.c_int
         L.nvfp4_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
         L.nvfp4_status_string.restype = ctypes.c_char_p
@@ -251,6 +256,30 @@ def pack_scales_tensor(sf_rowmajor, k: int, stream=None):
     if out.numel():
         pack_scales(sf_rowmajor.data_ptr(), rows, k, out.data_ptr(), stream)
     return out
+
+
+def pack_scales_batched(entries, stream=None, *, check: bool = True) -> int:
+    """nvfp4_pack_scales_batched: entries = [(sf_rowmajor_ptr, rows, k, sf_atoms_ptr), ...]."""
+    n = len(entries)
+    rows = (ctypes.c_int * max(n, 1))(*[int(e[1]) for e in entries])
+    ks = (ctypes.c_int * max(n, 1))(*[int(e[2]) for e in entries])
+    st = lib().nvfp4_pack_scales_batched(n, _ptr_array([e[0] for e in entries]), rows, ks,
+                                         _ptr_array([e[3] for e in entries]),
+                                         ctypes.c_void_p(_stream_handle(stream) or None))
+    if check:
+        _check(st)
+    return st
+
+
+def pack_scales_tensors(mats, stream=None):
+    """[(device uint8 [rows, k/16], k), ...] -> new device uint8 tensors in the
+    atom layout, all packed by one launch."""
+    import torch
+    outs = [torch.empty(scale_bytes(sf.shape[0], k), dtype=torch.uint8, device=sf.device) for sf, k in mats]
+    entries = [(sf.data_ptr(), sf.shape[0], k, out.data_ptr()) for (sf, k), out in zip(mats, outs) if out.numel()]
+    if entries:
+        pack_scales_batched(entries, stream)
+    return outs
 
 
 def device_status(stream=None) -> int:

@@ -530,6 +530,40 @@ int nvfp4_pack_scales(const void *sf_rowmajor, int rows, int k, void *sf_atoms, 
     return NVFP4_OK;
 }
 
+int nvfp4_pack_scales_batched(int count, const void *const *sf_rowmajor, const int *rows, const int *k,
+                              void *const *sf_atoms, nvfp4_stream_t stream) {
+    if (count < 0 || count > NVFP4_PACK_MAX_BATCH)
+        return fail(NVFP4_ERR_INVALID_ARG, "count = %d outside [0, %d]", count, NVFP4_PACK_MAX_BATCH);
+    if (count == 0)
+        return NVFP4_OK;
+    if (!sf_rowmajor || !rows || !k || !sf_atoms)
+        return fail(NVFP4_ERR_INVALID_ARG, "null array");
+    std::vector<const uint8_t *> src;
+    std::vector<uint8_t *> dst;
+    std::vector<int> rs, ks;
+    for (int i = 0; i < count; ++i) {
+        if (rows[i] < 0 || k[i] < 0)
+            return fail(NVFP4_ERR_INVALID_ARG, "entry %d: negative rows (%d) or k (%d)", i, rows[i], k[i]);
+        if (k[i] % 16 != 0)
+            return fail(NVFP4_ERR_UNSUPPORTED, "entry %d: k = %d is not a multiple of 16", i, k[i]);
+        if (rows[i] == 0 || k[i] == 0)
+            continue;
+        if (!sf_rowmajor[i] || !sf_atoms[i])
+            return fail(NVFP4_ERR_INVALID_ARG, "entry %d: null scale pointer", i);
+        if (!aligned16(sf_atoms[i]))
+            return fail(NVFP4_ERR_MISALIGNED, "entry %d: sf_atoms not 16-byte aligned", i);
+        src.push_back(static_cast<const uint8_t *>(sf_rowmajor[i]));
+        dst.push_back(static_cast<uint8_t *>(sf_atoms[i]));
+        rs.push_back(rows[i]);
+        ks.push_back(k[i]);
+    }
+    cudaError_t e = launch_pack_scales_batched((int)src.size(), src.data(), rs.data(), ks.data(), dst.data(),
+                                               reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "batched scale packer launch");
+    return NVFP4_OK;
+}
+
 int nvfp4_quantize_pack(const void *x, int x_dtype, int rows, int k, void *codes, void *sf_atoms,
                         nvfp4_stream_t stream) {
     if (rows < 0 || k < 0)

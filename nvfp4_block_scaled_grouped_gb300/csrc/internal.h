@@ -235,5 +235,9 @@ cudaError_t launch_quantize_pack(const void *x, bool bf16, int rows, int k, void
 
 // Packer launcher (pack_scales.cu).
 cudaError_t launch_pack_scales(const uint8_t *src, int rows, int k, uint8_t *dst, cudaStream_t stream);
+// Matrices per nvfp4_pack_scales_batched launch (kernel parameter budget).
+constexpr int kPackBatchMax = NVFP4_PACK_MAX_BATCH;
+cudaError_t launch_pack_scales_batched(int count, const uint8_t *const *src, const int *rows, const int *k,
+                                       uint8_t *const *dst, cudaStream_t stream);
 
 }  // namespace nvfp4

@@ -17,13 +17,13 @@
 namespace nvfp4 {
 namespace {
 
-__global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t *__restrict__ src, int rows, int k,
-                                                          uint8_t *__restrict__ dst, long long lines) {
+// Lines q0, q0 + step, ... of one matrix.
+__device__ __forceinline__ void pack_lines(const uint8_t *__restrict__ src, int rows, int k, uint8_t *__restrict__ dst,
+                                           long long lines, long long q0, long long step) {
     const int kbs = k / 16;
     const int k_atoms = (k + 63) / 64;
     const bool words = (kbs % 4) == 0 && (reinterpret_cast<uintptr_t>(src) % 4) == 0;
-    for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < lines;
-         q += (long long)gridDim.x * blockDim.x) {
+    for (long long q = q0; q < lines; q += step) {
         const long long atom = q >> 5;
         const int l = (int)(q & 31);
         const int row_block = (int)(atom / k_atoms);
@@ -50,6 +50,28 @@ __global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t *__restr
     }
 }
 
+__global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t *__restrict__ src, int rows, int k,
+                                                          uint8_t *__restrict__ dst, long long lines) {
+    pack_lines(src, rows, k, dst, lines, (long long)blockIdx.x * blockDim.x + threadIdx.x,
+               (long long)gridDim.x * blockDim.x);
+}
+
+// Several matrices in one launch: CTA row blockIdx.y packs matrix blockIdx.y.
+struct PackBatch {
+    const uint8_t *src[kPackBatchMax];
+    uint8_t *dst[kPackBatchMax];
+    int rows[kPackBatchMax];
+    int k[kPackBatchMax];
+};
+
+__global__ void __launch_bounds__(256) pack_scales_batched_kernel(const __grid_constant__ PackBatch b) {
+    const int i = blockIdx.y;
+    const int rows = b.rows[i], k = b.k[i];
+    const long long lines = (long long)((rows + 127) / 128) * ((k + 63) / 64) * 32;
+    pack_lines(b.src[i], rows, k, b.dst[i], lines, (long long)blockIdx.x * blockDim.x + threadIdx.x,
+               (long long)gridDim.x * blockDim.x);
+}
+
 }  // namespace
 
 cudaError_t launch_pack_scales(const uint8_t *src, int rows, int k, uint8_t *dst, cudaStream_t stream) {
@@ -66,6 +88,40 @@ cudaError_t launch_pack_scales(const uint8_t *src, int rows, int k, uint8_t *dst
     if (blocks > cap)
         blocks = cap;
     pack_scales_kernel<<<(unsigned)blocks, 256, 0, stream>>>(src, rows, k, dst, lines);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_scales_batched(int count, const uint8_t *const *src, const int *rows, const int *k,
+                                       uint8_t *const *dst, cudaStream_t stream) {
+    if (count <= 0)
+        return cudaSuccess;
+    if (count > kPackBatchMax)
+        return cudaErrorInvalidValue;
+    PackBatch b;
+    long long max_lines = 0, total_lines = 0;
+    for (int i = 0; i < count; ++i) {
+        b.src[i] = src[i];
+        b.dst[i] = dst[i];
+        b.rows[i] = rows[i];
+        b.k[i] = k[i];
+        const long long lines = (long long)((rows[i] + 127) / 128) * ((k[i] + 63) / 64) * 32;
+        max_lines = lines > max_lines ? lines : max_lines;
+        total_lines += lines;
+    }
+    if (max_lines == 0)
+        return cudaSuccess;
+    int device = 0, sms = 148;
+    cudaGetDevice(&device);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    // about 8 CTAs per SM over the whole batch, spread in proportion to the
+    // largest matrix (smaller ones finish early in their row)
+    long long per_row = (8LL * sms * max_lines + total_lines - 1) / total_lines;
+    const long long need = (max_lines + 255) / 256;
+    if (per_row > need)
+        per_row = need;
+    if (per_row < 1)
+        per_row = 1;
+    pack_scales_batched_kernel<<<dim3((unsigned)per_row, (unsigned)count), 256, 0, stream>>>(b);
     return cudaGetLastError();
 }
 

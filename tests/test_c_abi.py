@@ -138,3 +138,21 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(nv, "_LIB_PATH", tmp_path / "missing.so")
     with pytest.raises(RuntimeError, match="missing"):
         nv.lib()
+
+
+def test_pack_scales_batched_argument_errors(L):
+    """Every entry is checked on the host before anything is enqueued."""
+    vp = ctypes.c_void_p
+    f = L.nvfp4_pack_scales_batched
+    arr = lambda *v: (vp * len(v))(*[vp(x) if x else None for x in v])
+    ints = lambda *v: (ctypes.c_int * len(v))(*v)
+    assert f(0, None, None, None, None, None) == 0                                       # nothing to pack
+    assert f(-1, None, None, None, None, None) == -1
+    assert f(1025, None, None, None, None, None) == -1                                   # above NVFP4_PACK_MAX_BATCH
+    assert f(1, None, ints(4), ints(64), arr(0x20000), None) == -1                       # null array
+    src, dst = arr(0x10000, 0x11000), arr(0x20000, 0x21000)
+    assert f(2, arr(0x10000, 0x11000), ints(4, -1), ints(64, 64), dst, None) == -1       # negative rows
+    assert f(2, src, ints(4, 4), ints(64, 40), dst, None) == -2                          # k % 16
+    assert f(2, src, ints(4, 4), ints(64, 64), arr(0x20000, 0x21008), None) == -3        # misaligned output
+    assert f(2, arr(0x10000, 0), ints(4, 4), ints(64, 64), dst, None) == -1              # null pointer
+    assert f(2, arr(0, 0), ints(0, 4), ints(64, 0), arr(0, 0), None) == 0                # only empty entries

@@ -72,6 +72,22 @@ def test_pack_scales_matches_cpu_packer(nv, oracle_mod, rows, k):
     np.testing.assert_array_equal(got, oracle_mod.pack_scales(sf, k))
 
 
+def test_batched_packer_matches_cpu_packer(nv, oracle_mod):
+    """nvfp4_pack_scales_batched packs every matrix of a mixed batch (ragged
+    rows, K tails, empty entries, one large matrix) byte for byte as the CPU
+    packer does, padding included, in one launch."""
+    shapes = [(1, 32), (0, 64), (128, 64), (129, 96), (300, 256), (5, 0), (4096, 7168), (1000, 160), (77, 16)]
+    rng = np.random.default_rng(5)
+    mats = [rng.integers(0, 256, (r, k // 16), dtype=np.uint8) for r, k in shapes]
+    outs = nv.pack_scales_tensors([(torch.from_numpy(m).cuda(), k) for m, (_, k) in zip(mats, shapes)])
+    torch.cuda.synchronize()
+    for m, (r, k), out in zip(mats, shapes, outs):
+        if r == 0 or k == 0:
+            assert out.numel() == 0
+            continue
+        np.testing.assert_array_equal(out.cpu().numpy(), oracle_mod.pack_scales(m, k), err_msg=f"{(r, k)}")
+
+
 # ---------------------------------------------------------------- full parity, small shapes
 
 @pytest.mark.parametrize("block_n", [128, 256])
