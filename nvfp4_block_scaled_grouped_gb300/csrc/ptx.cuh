@@ -1,7 +1,7 @@
 // ptx.cuh -- inline-PTX wrappers for the sm_103a features the GEMM uses:
 // mbarriers, TMA (tensor and bulk copies), tensormap patching, tcgen05
-// (TMEM allocation, smem->TMEM copy, block-scaled MMA, TMEM loads, commits),
-// programmatic dependent launch. Written from the public PTX ISA.
+// (TMEM allocation, block-scaled MMA, TMEM loads and stores, commits).
+// Written from the public PTX ISA.
 #pragma once
 
 #include <cstdint>
@@ -97,20 +97,10 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     return p;
 }
 
-__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
-}
-
-__device__ __forceinline__ void prefetch_tmap(const void *tmap) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
 // Acquire side of a tensormap written through the generic proxy.
@@ -146,14 +136,6 @@ __device__ __forceinline__ void tmap_set_stride1(void *tmap, uint64_t stride_byt
                  : "memory");
 }
 
-// ---- programmatic dependent launch ---------------------------------------
-
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-__device__ __forceinline__ void griddep_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // ---- tcgen05 ----------------------------------------------------------------
 
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
@@ -186,12 +168,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                  : "memory");
 }
 
-// Copy a 32-row x 16-byte matrix from shared memory into TMEM lanes 0..31,
-// 4 columns, replicated into the other three 32-lane quarters.
-__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // D(tmem) (+)= A(smem) * B(smem) with per-16-element e4m3 scales read from TMEM.
 __device__ __forceinline__ void tc_mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
@@ -201,21 +177,6 @@ __device__ __forceinline__ void tc_mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc,
         "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
             d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
-        : "memory");
-}
-
-// 32 consecutive TMEM columns of this thread's lane (32x32b shape, x32).
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
-          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),
-          "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
-          "=r"(v[30]), "=r"(v[31])
-        : "r"(taddr)
         : "memory");
 }
 
@@ -231,13 +192,6 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&v)
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Write 4 consecutive TMEM columns of this thread's lane (32x32b shape, x4).
-__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint4 v) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
 
 // 16 / 32 consecutive columns of the warp's 32 lanes in one instruction.
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&v)[16]) {
@@ -310,17 +264,6 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
     d |= static_cast<uint64_t>(1024u >> 4) << 32;  // SBO: 8 rows x 128 B
     d |= static_cast<uint64_t>(1u) << 46;
     d |= static_cast<uint64_t>(2u) << 61;
-    return d;
-}
-
-// 32 rows x 16 bytes stored contiguously (one scale atom), no swizzle:
-// 8-row core matrices 128 bytes apart.
-__device__ __forceinline__ uint64_t sdesc_sf_atom(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>(128u >> 4) << 16;
-    d |= static_cast<uint64_t>(128u >> 4) << 32;
-    d |= static_cast<uint64_t>(1u) << 46;
     return d;
 }
 
