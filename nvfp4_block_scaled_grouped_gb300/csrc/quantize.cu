@@ -13,12 +13,12 @@
 //   amax = max|x|;  sf = e4m3fn(amax / 6), round to nearest even, saturating
 //   at 448;  code = e2m1(x / dec(sf)), round to nearest even, saturating at
 //   6, sign of x kept;  all codes +0 when dec(sf) == 0.
-// amax / 6 is an IEEE fp32 division (__fdiv_rn) followed by an exact
-// conversion to e4m3. The e2m1 codes come from the hardware conversion
-// (cvt.rn.satfinite.e2m1x2.f32) of quotients x / dec that are exact on the
-// rounding boundaries of the e2m1 grid and within an ulp elsewhere (see
-// quantize16): for bf16 and fp16 inputs that decides every code as the exact
-// quotient would.
+// amax / 6 is formed exactly on every e4m3 rounding midpoint and within
+// about 2 ulps elsewhere, then converted exactly to e4m3. The e2m1 codes come
+// from the hardware conversion (cvt.rn.satfinite.e2m1x2.f32) of quotients
+// x / dec that are exact on the rounding boundaries of the e2m1 grid and
+// within about 2 ulps elsewhere (see quantize16): for bf16 and fp16 inputs
+// that decides the scale and every code as the exact quotients would.
 //
 // Layout of the work: a unit is one row and 32 consecutive scale blocks (512
 // K-elements); a warp takes a unit with one lane per 16-element block, so each
@@ -105,35 +105,53 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&q)[8]) {
     return out;
 }
 
+// x / d (d > 0) from an estimate r of 1/d by one corrected-quotient step of
+// Markstein's division method: q0 = x * r, q = q0 + (x - q0 * d) * r, the
+// residual x - q0 * d exact (FMA). With r within a few ulps of 1/d, q is
+// exactly x / d whenever that quotient is representable (the correction
+// moves q0 by (x/d - q0)(1 + O(ulp)), far less than half an ulp away from the
+// exact value) and within about 2 ulps of it otherwise.
+__device__ __forceinline__ float div_corrected(float x, float d, float r) {
+    const float q0 = x * r;
+    return fmaf(fmaf(-q0, d, x), r, q0);
+}
+
+// Hardware reciprocal estimate (PTX rcp.approx, about 1 ulp); d here is an
+// e4m3 value in [2^-9, 448], a normal fp32 number.
+__device__ __forceinline__ float rcp_estimate(float d) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+    return r;
+}
+
 // Quantise one 16-element block: its e4m3 scale code, and its 16 e2m1 codes
 // packed into 8 bytes (element j in bits 4j..4j+3).
 //
-// The quotients x / dec are formed as q0 = x * r with r = 1/dec rounded, then
-// one correction q = q0 + (x - q0 * dec) * r with the residual exact (FMA).
-// This lands exactly on every quotient that is an e2m1 rounding boundary
-// (x = t * dec), so the ties are decided by the conversion's
-// round-to-nearest-even; every other quotient is within an ulp of the exact
-// one, and for bf16 / fp16 inputs no such quotient lies within 2^-12 (relative)
-// of a boundary, so the codes are those of the exact quotient.
+// amax / 6 and the quotients x / dec come from div_corrected: exact on every
+// quotient that is representable -- in particular on every e4m3 rounding
+// midpoint amax / 6 and every e2m1 rounding boundary x / dec = t -- so those
+// ties are decided by round-to-nearest-even as for the exact quotient; every
+// other quotient is within about 2 ulps of the exact one, and for bf16 / fp16
+// inputs none lies within 2^-10 (relative) of a boundary, so the scale and the
+// codes are those of the exact quotients.
 __device__ __forceinline__ uint32_t quantize16(const float (&f)[16], uint2 &packed) {
     float amax = 0.0f;
 #pragma unroll
     for (int j = 0; j < 16; ++j)
         amax = fmaxf(amax, fabsf(f[j]));
-    const uint32_t sc = e4m3_code(__fdiv_rn(amax, 6.0f));
+    const uint32_t sc = e4m3_code(div_corrected(amax, 6.0f, 1.0f / 6.0f));
     const float dec = e4m3_decode(sc);
     uint32_t w[2] = {0u, 0u};
     if (dec != 0.0f) {
-        const float r = __frcp_rn(dec);
+        const float r = rcp_estimate(dec);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             float q[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const float x = f[8 * h + j];
-                const float q0 = x * r;
                 // (the correction turns x = -0 into +0; the quotient has x's sign)
-                q[j] = copysignf(fmaf(fmaf(-q0, dec, x), r, q0), x);
+                q[j] = copysignf(div_corrected(x, dec, r), x);
             }
             w[h] = cvt_e2m1x8(q);
         }
