@@ -43,23 +43,18 @@ namespace {
 constexpr int kQuantThreads = 256;  // 8 warps per CTA
 constexpr int kUnitBlocks = 32;     // scale blocks per unit (one per lane)
 
-// e4m3fn code of s >= 0 (finite), round to nearest even, 448 for s >= 448.
+// e4m3fn code of s >= 0 (finite), round to nearest even, 448 for s >= 448:
+// the hardware conversion (cvt.rn.satfinite.e4m3x2.f32, round to nearest
+// even on the e4m3 grid including its subnormals, saturating at the largest
+// finite value), low byte.
 __device__ __forceinline__ uint32_t e4m3_code(float s) {
-    if (!(s < 448.0f))
-        return 0x7Eu;
-    if (s < 0.015625f)  // below 2^-6: the subnormal grid, step 2^-9 (s * 512 is exact)
-        return (uint32_t)__float2int_rn(s * 512.0f);  // 0..8; 8 is 2^-6, code 0x08
-    const uint32_t bits = __float_as_uint(s);
-    const int e = (int)(bits >> 23) - 127;                         // -6..8
-    const float mant = __uint_as_float((bits & 0x007FFFFFu) | 0x3F800000u);  // s / 2^e, in [1, 2)
-    int m = __float2int_rn((mant - 1.0f) * 8.0f);                  // exact operands; 0..8
-    int ee = e + 7;
-    if (m == 8) {
-        m = 0;
-        ++ee;
-    }
-    const uint32_t code = (uint32_t)((ee << 3) | m);
-    return code > 0x7Eu ? 0x7Eu : code;
+    uint32_t out;
+    asm("{\n\t.reg .b16 h;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 h, %2, %1;\n\t"
+        "cvt.u32.u16 %0, h;\n\t}"
+        : "=r"(out)
+        : "f"(s), "f"(0.0f));
+    return out & 0xFFu;
 }
 
 // Value of a non-negative e4m3fn code (not NaN), exact in fp32.
