@@ -5,7 +5,7 @@ One step = one grouped call (one persistent GEMM kernel) over the
 workload's seeded synthetic inputs, resident in HBM, L2 flushed between timed
 calls. Prints ONE JSON line (rank 0).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload prefill]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
   python bench.py --api device ...        # the device-resident group-table entry point
   python bench.py --op quantize ...       # quantise-and-pack of the workload's activations
@@ -47,7 +47,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", default="decode", choices=list(WORKLOAD_TEXT))
+    ap.add_argument("--workload", default="prefill", choices=list(WORKLOAD_TEXT))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--tile-n", type=int, default=0, help="GEMM tile N (0 = library default)")
     ap.add_argument("--api", choices=["host", "device"], default="host",
@@ -215,32 +215,85 @@ def gpu_uuid(dev_index):
 
 # ------------------------------------------------------------------ the oracle legs (CPU)
 
-def oracle_sample(prob, seconds, seed=1234):
+def host_cores() -> int:
+    """Host cores this process may run on (the oracle's thread count when all are used)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(prob, seconds, threads=0):
     """Time the CPU oracle on a column slice of every non-empty group, sized to
-    take about `seconds` of wall time. Returns (flops, wall_s, cores, text)."""
+    take about `seconds` of wall time (`threads` OpenMP threads, 0 = all).
+    Returns (flops, wall_s, threads_used, text, fraction of C's outputs)."""
     import numpy as np
     from oracle import oracle
 
+    threads = threads or host_cores()
     groups = [(g, s) for g, s in enumerate(prob.problem_sizes) if s[0] > 0 and s[1] > 0 and s[2] > 0]
+    outputs = sum(m * n for _, (m, n, _, _) in groups)
 
     def run(cols_per_group):
-        flops = 0.0
+        flops, done = 0.0, 0
         t0 = time.perf_counter()
         for g, (m, n, k, _) in groups:
             c = min(cols_per_group, n)
             rows = np.repeat(np.arange(m, dtype=np.int32), c)
             cols = np.tile(np.arange(c, dtype=np.int32), m)
-            oracle.gemm_sampled(m, n, k, prob.A[g], prob.B[g], prob.SFA[g], prob.SFB[g], rows, cols)
+            oracle.gemm_sampled(m, n, k, prob.A[g], prob.B[g], prob.SFA[g], prob.SFB[g], rows, cols,
+                                threads=threads)
             flops += 2.0 * m * c * k
-        return flops, time.perf_counter() - t0
+            done += m * c
+        return flops, time.perf_counter() - t0, done
 
-    f0, t0 = run(2)
+    _, t0, _ = run(2)
     per_col = t0 / 2
     cols = int(max(2, min(max(s[1] for _, s in groups), seconds / max(per_col, 1e-9))))
-    flops, wall = run(cols)
+    flops, wall, done = run(cols)
+    frac = done / outputs
     text = (f"all rows x the first {cols} columns of each of the {len(groups)} non-empty groups "
-            f"({flops / 2:.3g} multiply-adds, fp64, full k)")
-    return flops, wall, oracle.max_threads(), text
+            f"({flops / 2:.3g} multiply-adds, fp64, full k; {100 * frac:.3g}% of C's outputs) "
+            f"on {threads} thread{'s' if threads > 1 else ''}")
+    return flops, wall, threads, text, frac
+
+
+def oracle_full(prob, threads):
+    """Time the oracle's full C (every output of every group). Returns (flops, wall_s)."""
+    from oracle import oracle
+    t0 = time.perf_counter()
+    oracle.grouped_gemm(prob.problem_sizes, prob.A, prob.B, prob.SFA, prob.SFB, threads=threads)
+    return float(prob.flops()), time.perf_counter() - t0
+
+
+def cpu_baseline_leg(prob, seconds):
+    """The oracle as it stands on the host cores: full C when the slice rate
+    says it ends within ~3x `seconds`, else a column slice (with the fraction
+    of C it covers); plus single-thread figures on the two small task configs
+    (the two-group tiny call in full, a slice of the ragged call)."""
+    from nvfp4_block_scaled_grouped_gb300 import workloads
+    from oracle import oracle
+
+    cores = host_cores()
+    f, w, _, text, frac = oracle_sample(prob, min(seconds, 3.0), threads=cores)
+    full_est = w / max(frac, 1e-12)
+    if full_est <= 3.0 * seconds:
+        f, w = oracle_full(prob, cores)
+        text, frac = f"full C ({f / 2:.3g} multiply-adds, fp64) on {cores} threads", 1.0
+    elif seconds > 3.0:
+        f, w, _, text, frac = oracle_sample(prob, seconds, threads=cores)
+    single = {}
+    tiny = workloads.make_problem("tiny", seed=0)
+    tf, tw = oracle_full(tiny, 1)
+    single["tiny"] = {"value": tf / tw / 1e12, "unit": "TFLOP/s", "wall_s": tw, "fraction_of_C": 1.0,
+                      "sample": "full C of G=2: (128,128,256), (64,256,256), 1 thread"}
+    rag = workloads.make_problem("ragged", seed=0)
+    rf, rw, _, rtext, rfrac = oracle_sample(rag, 2.0, threads=1)
+    single["ragged"] = {"value": rf / rw / 1e12, "unit": "TFLOP/s", "wall_s": rw, "fraction_of_C": rfrac,
+                        "sample": rtext}
+    return {"value": f / w / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": text,
+            "wall_s": w, "fraction_of_C": frac, "full_C": frac == 1.0,
+            "full_C_estimate_s": full_est if frac < 1.0 else w, "single_core": single}
 
 
 def reference_arm(args, rank, world):
@@ -255,7 +308,7 @@ def reference_arm(args, rank, world):
     flops_l, wall_l = [], []
     text, cores = "", 0
     for _ in range(args.steps):
-        f, w, cores, text = oracle_sample(prob, per_step)
+        f, w, cores, text, frac = oracle_sample(prob, per_step)
         flops_l.append(f)
         wall_l.append(w)
     value = sum(flops_l) / sum(wall_l) / 1e12
@@ -265,7 +318,7 @@ def reference_arm(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(args, prob),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"per step: {text}"},
+                         "sample": f"per step: {text}", "fraction_of_C": frac},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -462,9 +515,7 @@ def gpu_arm(args, rank, world, local_rank):
 
     cpu = None
     if not args.no_cpu_baseline:
-        f, w, cores, text = oracle_sample(prob, args.cpu_seconds)
-        cpu = {"value": f / w / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": text, "wall_s": w}
+        cpu = cpu_baseline_leg(prob, args.cpu_seconds)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

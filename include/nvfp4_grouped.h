@@ -174,14 +174,25 @@ int nvfp4_grouped_gemm_device(int group_count, const nvfp4_problem_size *problem
  *    about 24 KiB) is one fixed array in the library's device memory, which
  *    every GPU that loads the library holds until the process exits. The call
  *    never calls cudaMalloc, cudaFree or any other allocating routine;
+ *  - the array has no room for the fp32 partial tiles of the split-K
+ *    schedule, so calls always run whole output tiles. Calls with fewer tiles
+ *    than about one and a half waves of the GPU are then slower than through
+ *    nvfp4_grouped_gemm (measured on GB300: the 8-group decode shape, m
+ *    40..192, n 4096, k 7168, 47.6 us instead of 39.6 us for the same
+ *    kernel). Results are the same within the fp16 rounding of a different
+ *    summation order;
  *  - every call on a device shares that array and it keeps the previous
- *    call's contents (each call rewrites what it reads and clears the status
- *    word first). Calls whose work overlaps on the GPU -- on different
+ *    call's contents (each call rewrites what it reads and clears its call
+ *    counters first). Calls whose work overlaps on the GPU -- on different
  *    streams, or from different host threads without ordering -- race on it:
  *    issue them in one stream or otherwise serialise them;
+ *  - the status word in the array collects the bits of every call on the
+ *    device until nvfp4_device_status (any stream) reads and clears it;
  *  - the first call on a device sets that device up (looks up the array's
  *    device address, encodes the TMA descriptor templates, sets kernel
  *    attributes); make that first call before any stream capture begins.
+ *    The address stays cached for the process: after cudaDeviceReset the
+ *    entry point must not be used again.
  */
 int nvfp4_grouped_gemm_noalloc(int group_count, const nvfp4_problem_size *problem_sizes,
                                const void *const *A, const void *const *B,
@@ -262,8 +273,9 @@ int nvfp4_quantize_pack(const void *x, int x_dtype, int rows, int k, void *codes
                         nvfp4_stream_t stream);
 
 /*
- * nvfp4_device_status -- read and clear the device-side status word of the
- * (current device, stream) workspace. Synchronises `stream`. *status receives
+ * nvfp4_device_status -- read and clear the device-side status words of the
+ * (current device, stream) workspace and of the current device's
+ * nvfp4_grouped_gemm_noalloc array. Synchronises `stream`. *status receives
  * NVFP4_OK; NVFP4_ERR_TIMEOUT if a kernel of an earlier call gave up a
  * bounded wait (its C is then incomplete); or NVFP4_ERR_INVALID_ARG if an
  * nvfp4_grouped_gemm_device call skipped a group that breaks the group rules.

@@ -595,27 +595,36 @@ int nvfp4_device_status(nvfp4_stream_t stream, int *status) {
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaGetDevice");
-    void *ws_base = nullptr;
+    // The status words to read: the (device, stream) workspace's, and the
+    // static array of nvfp4_grouped_gemm_noalloc (one per device, shared by
+    // every stream) once a call has set it up.
+    uint32_t *words[2] = {nullptr, nullptr};
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         auto it = g_workspaces.find(std::make_pair(device, reinterpret_cast<cudaStream_t>(stream)));
-        if (it == g_workspaces.end())
-            return NVFP4_OK;
-        ws_base = it->second.base;
+        if (it != g_workspaces.end())
+            words[0] = workspace_view(it->second.base, NVFP4_MAX_GROUPS).status;
     }
-    const WorkspaceView ws = workspace_view(ws_base, NVFP4_MAX_GROUPS);
+    if (void *na = noalloc_workspace_if_ready(device))
+        words[1] = workspace_view(na, NVFP4_NOALLOC_MAX_GROUPS).status;
     uint32_t word = 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    e = cudaMemcpyAsync(&word, ws.status, sizeof(word), cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess)
-        e = cudaStreamSynchronize(s);
-    if (e == cudaSuccess && word != 0) {
-        e = cudaMemsetAsync(ws.status, 0, sizeof(word), s);
+    for (uint32_t *w : words) {
+        if (!w)
+            continue;
+        uint32_t v = 0;
+        e = cudaMemcpyAsync(&v, w, sizeof(v), cudaMemcpyDeviceToHost, s);
         if (e == cudaSuccess)
             e = cudaStreamSynchronize(s);
+        if (e == cudaSuccess && v != 0) {
+            e = cudaMemsetAsync(w, 0, sizeof(v), s);
+            if (e == cudaSuccess)
+                e = cudaStreamSynchronize(s);
+        }
+        if (e != cudaSuccess)
+            return cuda_fail(e, "reading the device status word");
+        word |= v;
     }
-    if (e != cudaSuccess)
-        return cuda_fail(e, "reading the device status word");
     if (word & kStatusTimeoutMask) {
         *status = NVFP4_ERR_TIMEOUT;
         fail(NVFP4_ERR_TIMEOUT,

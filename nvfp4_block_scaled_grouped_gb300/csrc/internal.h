@@ -229,6 +229,10 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
 int launch_device_table(int group_count, const DeviceTable &dt, int block_n, void *ws_base, int capacity,
                         int slots, WorkspaceState *state, cudaStream_t stream);
 
+// The static scratch array of nvfp4_grouped_gemm_noalloc on `device` once a
+// call has set it up there, else null (noalloc.cu).
+void *noalloc_workspace_if_ready(int device);
+
 // Quantise-and-pack launcher (quantize.cu).
 cudaError_t launch_quantize_pack(const void *x, bool bf16, int rows, int k, void *codes, void *sf_atoms,
                                  cudaStream_t stream);

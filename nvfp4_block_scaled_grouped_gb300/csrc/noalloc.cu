@@ -28,9 +28,13 @@ constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void *g_noalloc_ptr[kMaxDevices] = {};
 
+}  // namespace
+
 // Device address of g_noalloc_workspace on `device` (the current device).
 // In host code the array's name is only a host-side stand-in, so the address
-// is looked up once per device and cached.
+// is looked up once per device, at the device's first call, and cached; after
+// a cudaDeviceReset the cached address is stale, so the entry point must not
+// be used again in that process.
 int noalloc_workspace(int device, void **out) {
     if (device < 0 || device >= kMaxDevices)
         return fail(NVFP4_ERR_UNSUPPORTED, "device ordinal %d out of range", device);
@@ -46,7 +50,15 @@ int noalloc_workspace(int device, void **out) {
     return NVFP4_OK;
 }
 
-}  // namespace
+// The static array's address on `device` if a call has set it up there, else
+// null (nothing is looked up or allocated).
+void *noalloc_workspace_if_ready(int device) {
+    if (device < 0 || device >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    return g_noalloc_ptr[device];
+}
+
 }  // namespace nvfp4
 
 using namespace nvfp4;
@@ -74,9 +86,12 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int group_count, const nvfp4_problem_s
     if (s != NVFP4_OK)
         return s;
     // The array keeps the previous call's contents. Each call rewrites the
-    // descriptors it reads; the header (status word and the counter the
-    // descriptor patching counts up) must start at zero.
-    e = cudaMemsetAsync(ws, 0, 128, reinterpret_cast<cudaStream_t>(stream));
+    // descriptors it reads; the call counters of the header (bytes 64..127:
+    // the descriptor-publication counter, the count of CTAs past it, the
+    // epoch) must start at zero. The status word (byte 0) is left alone: it
+    // collects the bits of every call until nvfp4_device_status reads and
+    // clears it.
+    e = cudaMemsetAsync(static_cast<uint8_t *>(ws) + 64, 0, 64, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "clearing the static workspace header");
     WorkspaceState state;  // empty slot cache: every descriptor is patched

@@ -46,3 +46,23 @@ def assert_parity(gpu, ref, what: str = "") -> None:
         first = [tuple(int(v) for v in b) for b in bad[:8]]
         vals = [(float(gpu[b]), float(ref[b])) for b in first]
         raise AssertionError(f"{what}: {len(bad)} of {ok.size} outside tolerance; first {first}: {vals}")
+
+
+def block_samples(rng, m: int, n: int, block: int = 32, per_block: int = 2, edges: bool = True):
+    """Output coordinates that reach every `block` x `block` cell of an m x n C:
+    `per_block` random (row, col) pairs inside each cell (clipped to the
+    matrix), plus, with `edges`, the whole last row and last column (the M and N
+    tails). Every (tile, column chunk, TMEM lane quarter) of any tiling whose
+    tile sides are multiples of `block` holds at least one sample."""
+    rb = -(-m // block)
+    cb = -(-n // block)
+    r0 = np.repeat(np.arange(rb) * block, cb * per_block)
+    c0 = np.tile(np.repeat(np.arange(cb) * block, per_block), rb)
+    rows = r0 + rng.integers(0, block, r0.size)
+    cols = c0 + rng.integers(0, block, c0.size)
+    rows = np.minimum(rows, m - 1)
+    cols = np.minimum(cols, n - 1)
+    if edges:
+        rows = np.concatenate([rows, np.full(n, m - 1), np.arange(m)])
+        cols = np.concatenate([cols, np.arange(n), np.full(m, n - 1)])
+    return rows.astype(np.int32), cols.astype(np.int32)

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-from parity import assert_parity
+from parity import assert_parity, block_samples
 
 pytestmark = pytest.mark.gpu
 
@@ -92,8 +92,7 @@ def test_device_table_full_size_sampled(nv, oracle_mod, name):
             continue
         c = got[g]
         assert not np.isnan(c.astype(np.float32)).any(), f"{name} group {g}"
-        rows = rng.integers(0, m, 512).astype(np.int32)
-        cols = rng.integers(0, n, 512).astype(np.int32)
+        rows, cols = block_samples(rng, m, n)
         ref = oracle_mod.gemm_sampled(m, n, k, prob.A[g], prob.B[g], prob.SFA[g], prob.SFB[g], rows, cols)
         assert_parity(c[rows, cols], ref, f"{name} group {g}")
     # the host-table entry point gives the same bits (same kernel, same schedule rule)

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from parity import assert_parity
+from parity import assert_parity, block_samples
 
 pytestmark = pytest.mark.gpu
 
@@ -196,15 +196,13 @@ def test_unit_scale_single_element(nv):
 # ---------------------------------------------------------------- full-size workloads, sampled
 
 def _samples(rng, m, n, count=1024):
-    rows = list(rng.integers(0, m, count))
-    cols = list(rng.integers(0, n, count))
-    last_cols = np.arange(max(0, n - 256), n)
-    rows += [m - 1] * len(last_cols)
-    cols += list(last_cols)
-    last_rows = np.arange(max(0, m - 256), m)
-    rows += list(last_rows)
-    cols += [n - 1] * len(last_rows)
-    return np.array(rows, np.int32), np.array(cols, np.int32)
+    """Two random outputs in every 32 x 32 cell of C (so every tile, column
+    chunk and TMEM lane quarter of the kernel's tiling is reached), the last
+    row and column, and `count` more anywhere."""
+    br, bc = block_samples(rng, m, n)
+    rows = np.concatenate([br, rng.integers(0, m, count)])
+    cols = np.concatenate([bc, rng.integers(0, n, count)])
+    return rows.astype(np.int32), cols.astype(np.int32)
 
 
 _PROBLEMS = {}
@@ -242,6 +240,20 @@ def test_full_size_sampled(nv, oracle_mod, monkeypatch, name, block_n, split):
     torch.cuda.synchronize()
     for g, c in enumerate(dp.c_host()):
         np.testing.assert_array_equal(c.view(np.uint16), got[g].view(np.uint16))
+
+
+@pytest.mark.parametrize("name", ["decode", "ragged"])
+def test_full_size_full_c(nv, oracle_mod, name):
+    """Every output of the full-size decode and ragged calls (library-chosen
+    tile width and schedule) against the oracle's full C."""
+    prob = _workload(name)
+    _, got = _run(nv, prob, 256)
+    ref = _oracle_full(oracle_mod, prob)
+    for g, ((m, n, k, _), c, r) in enumerate(zip(prob.problem_sizes, got, ref)):
+        if m == 0 or n == 0:
+            assert c.size == 0
+            continue
+        assert_parity(c, r, f"{name} group {g} (full C)")
 
 
 def test_two_streams_concurrently(nv, oracle_mod):
