@@ -40,6 +40,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
 struct DeviceState {
     bool ready = false;
     int sm_count = 0;
+    int pairs = 0;            // CTA pairs of the pair kernel resident at once (0: not used)
     CUtensorMap tmpl_a;       // box 128 B x 128 rows
     CUtensorMap tmpl_b128;    // box 128 B x 128 rows
     CUtensorMap tmpl_b256;    // box 128 B x 256 rows
@@ -123,6 +124,9 @@ int device_state(int device, void *any_device_buffer, DeviceState **out) {
         e = prepare_gemm_kernels(device);
         if (e != cudaSuccess)
             return cuda_fail(e, "cudaFuncSetAttribute");
+        st.pairs = pair_capacity(device);
+        if (st.pairs > st.sm_count / 2)
+            st.pairs = st.sm_count / 2;
         st.ready = true;
     }
     *out = &st;
@@ -245,6 +249,14 @@ int split_override() {
     return -1;
 }
 
+// NVFP4_PAIR=1 selects the CTA-pair kernel for calls that run whole tiles.
+int pair_override() {
+    const char *s = std::getenv("NVFP4_PAIR");
+    if (s && *s)
+        return std::atoi(s) == 1 ? 1 : 0;
+    return -1;
+}
+
 // Whether `stream` is capturing into a CUDA graph (the launch is then
 // replayed later, possibly after other calls changed the descriptor slots).
 bool capturing(cudaStream_t stream) {
@@ -259,7 +271,9 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaGetDevice");
-    long long total_work = 0;
+    // schedule units of the one-CTA tiling (128 x block_n tiles) and of the
+    // CTA-pair tiling (256 x 256 tiles)
+    long long total_work = 0, pair_tiles = 0, pair_work = 0;
     for (int g = 0; g < group_count; ++g) {
         const GroupArgs &a = args[g];
         if (a.m <= 0 || a.n <= 0)
@@ -268,12 +282,15 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
             (long long)((a.m + kBlockM - 1) / kBlockM) * ((a.n + block_n - 1) / block_n) * (long long)a.l;
         const long long kt = (a.k + kBlockK - 1) / kBlockK;
         total_work += tiles * (kt > 1 ? kt : 1);
+        const long long ptiles = (long long)((a.m + 2 * kBlockM - 1) / (2 * kBlockM)) * ((a.n + 255) / 256) * a.l;
+        pair_tiles += ptiles;
+        pair_work += ptiles * (kt > 1 ? kt : 1);
     }
     if (total_work > 0x7fffffffLL)
         return fail(NVFP4_ERR_UNSUPPORTED, "more than 2^31 - 1 k-tiles in one call");
     DeviceState *st = nullptr;
     GemmLaunch cfg;
-    int desc_maps = 0;
+    int desc_maps = 0, b_box = block_n;
     const bool graph = capturing(stream);
     // One lock over set-up, launch and bookkeeping: calls that share a
     // workspace must reach the GPU in the order their descriptor-cache
@@ -296,9 +313,22 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
             cfg.grid = (int)(total_work < sms ? total_work : sms);
         else
             cfg.grid = sms;  // whole waves use every SM
+        // CTA pairs (256 x 256 tiles, whole tiles only): only when forced
+        // with NVFP4_PAIR=1, and not with a split schedule forced.
+        const int pmode = pair_override();
+        cfg.pair = block_n == 256 && st->pairs > 0 && pmode == 1 && pair_work <= 0x7fffffffLL && forced <= 0;
+        if (cfg.pair) {
+            cfg.split = 0;
+            cfg.split_tile = (int)pair_tiles;
+            cfg.grid = 2 * (int)(pair_tiles < st->pairs ? pair_tiles : st->pairs);
+            total_tiles = pair_tiles;
+            total_work = pair_work;
+        }
         if (group_count > kMediumGroups && prefix_slots < cfg.grid)
             return fail(NVFP4_ERR_UNSUPPORTED, "workspace has %d CTA slots, the launch needs %d", prefix_slots,
                         cfg.grid);
+        // rows of B per TMA box: a CTA of a pair loads half of a 256-row tile
+        b_box = cfg.pair ? 128 : block_n;
         // Descriptors to patch: those whose region-0 slot does not already
         // hold this group's pointer and shape (region 0 is written only by
         // this workspace's eager calls, in stream order). A captured launch
@@ -313,7 +343,7 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
             a.patch = 0;
             if (a.m <= 0 || a.n <= 0 || a.k <= 0)
                 continue;
-            const DescKey ka{a.a, (int32_t)a.l * a.m, a.k, kBlockM}, kb{a.b, (int32_t)a.l * a.n, a.k, block_n},
+            const DescKey ka{a.a, (int32_t)a.l * a.m, a.k, kBlockM}, kb{a.b, (int32_t)a.l * a.n, a.k, b_box},
                 ks{a.sfb, (int32_t)a.l * ((a.n + kBlockM - 1) / kBlockM), a.k, 2};
             if (graph || !(state->descs[kDescPerGroup * g] == ka)) {
                 a.patch |= 1;
@@ -341,7 +371,7 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
     WorkspaceView ws = workspace_view(ws_base, capacity, prefix_slots, partial_slots, regions);
     if (graph && regions > 1)
         ws = second_region(ws);
-    const void *tmpl_b = block_n == 256 ? (const void *)&st->tmpl_b256 : (const void *)&st->tmpl_b128;
+    const void *tmpl_b = b_box == 256 ? (const void *)&st->tmpl_b256 : (const void *)&st->tmpl_b128;
     e = launch_grouped(cfg, args, ws, &st->tmpl_a, tmpl_b, &st->tmpl_sfb, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "grouped GEMM launch");  // nothing ran, no slot was written
@@ -352,7 +382,7 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
         if (a.patch & 1)
             state->descs[kDescPerGroup * g] = DescKey{a.a, (int32_t)a.l * a.m, a.k, kBlockM};
         if (a.patch & 2)
-            state->descs[kDescPerGroup * g + 1] = DescKey{a.b, (int32_t)a.l * a.n, a.k, block_n};
+            state->descs[kDescPerGroup * g + 1] = DescKey{a.b, (int32_t)a.l * a.n, a.k, b_box};
         if (a.patch & 4)
             state->descs[kDescPerGroup * g + 2] =
                 DescKey{a.sfb, (int32_t)a.l * ((a.n + kBlockM - 1) / kBlockM), a.k, 2};
@@ -383,6 +413,7 @@ int launch_device_table(int group_count, const DeviceTable &dt, int block_n, voi
     cfg.capacity = capacity;
     cfg.timeout_ns = watchdog_ns();
     cfg.device_table = true;
+    cfg.pair = false;
     cfg.dt = dt;
     (void)state;  // region 0 and its host cache are left alone
     const WorkspaceView ws = second_region(workspace_view(ws_base, capacity, slots, slots, 2));

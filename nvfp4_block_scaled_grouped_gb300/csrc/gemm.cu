@@ -81,13 +81,19 @@ namespace {
 
 constexpr int kPartialChunkBytes = 8 * kBlockM * 16;  // one 32-column chunk of an fp32 partial tile
 
-template <int BN, int CAP>
+// PAIR: a cluster of two CTAs computes 256 x BN tiles with cta_group::2 MMAs
+// (M = 256): each CTA stages its own 128 rows of A and its half (BN / 2 rows)
+// of B, and holds its 128 rows of the accumulator.
+template <int BN, int CAP, bool PAIR = false>
 struct Cfg {
     static_assert(BN == 128 || BN == 256, "BLOCK_N");
-    static constexpr int kStages = (BN == 128) ? 6 : 4;
+    static_assert(!PAIR || BN == 256, "CTA pairs use 256-column tiles");
+    static constexpr int kTileM = PAIR ? 2 * kBlockM : kBlockM;    // rows of C per schedule tile
+    static constexpr int kBRows = PAIR ? BN / 2 : BN;              // rows of B this CTA stages
+    static constexpr int kStages = PAIR ? 5 : ((BN == 128) ? 6 : 4);
     static constexpr int kAccStages = (BN == 128) ? 2 : 1;
     static constexpr int kABytes = kBlockM * 128;                  // 128 rows x 256 fp4
-    static constexpr int kBBytes = BN * 128;                       // BN rows x 256 fp4
+    static constexpr int kBBytes = kBRows * 128;                   // kBRows rows x 256 fp4
     static constexpr int kSfaBytes = 4 * kSfAtomBytes;             // 4 atoms (one per k-block)
     static constexpr int kSfbRowBlocks = BN / 128;
     static constexpr int kSfbBytes = kSfbRowBlocks * 4 * kSfAtomBytes;
@@ -108,7 +114,7 @@ struct Cfg {
     // accumulator barriers from 0, scratch from 176, scales-landed per stage
     // from 384
     static constexpr int kBarrierBytes = 448;
-    static_assert((3 * kStages + 2 * kAccStages) * 8 <= 176 && kStages <= 8, "barrier area");
+    static_assert(((PAIR ? 4 : 3) * kStages + 2 * kAccStages) * 8 <= 176 && kStages <= 8, "barrier area");
     static constexpr int kEpiStageBytes = 32 * 64;                 // per epilogue warp: 32 rows x 32 fp16
     // A finishing CTA receives the next piece's partial tile in ring stages,
     // kPartialChunksPerStage 16 KiB chunks (32 columns x 128 rows fp32) per
@@ -123,7 +129,8 @@ struct Cfg {
     static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kBarrierBytes + 4 * kEpiStageBytes +
                                          (kSmemPrefix ? 2 * sizeof(int32_t) * kPrefixInts : 0);
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    static constexpr uint32_t kIdesc = ptx::idesc_mxf4nvf4(kBlockM, BN);
+    static constexpr uint32_t kIdesc = ptx::idesc_mxf4nvf4(kTileM, BN);
+    static constexpr int kCtaGroup = PAIR ? 2 : 1;
 };
 
 // DEV: the group table is the caller's device arrays (`dt`), else `groups`.
@@ -189,7 +196,9 @@ __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b
 // Derived sizes of one group (m, n, k >= 0).
 struct GInfo {
     int m, n, k, l;
-    int tiles_m, tiles_mn;    // ceil(m / 128), ceil(m / 128) * ceil(n / BN) (0 for an empty group)
+    int tiles_m, tiles_mn;    // ceil(m / TM), ceil(m / TM) * ceil(n / BN) (0 for an empty group), TM the
+                              // schedule tile's rows (128, or 256 for CTA pairs)
+    int sf_row_blocks_a;      // ceil(m / 128): 128-row scale blocks of A
     int tiles;                // tiles_mn * l
     int k_tiles, k_blocks;    // ceil(k / 256), ceil(k / 64)
     int work_tiles;           // max(k_tiles, 1): schedule units per output tile
@@ -199,21 +208,22 @@ struct GInfo {
     void *c;
 };
 
-template <int BN>
+template <int BN, bool PAIR = false>
 __device__ __forceinline__ GInfo group_info(const GroupArgs &a) {
     GInfo g;
     g.m = a.m;
     g.n = a.n;
     g.k = a.k;
     g.l = a.l;
-    g.tiles_m = ceil_div_i(a.m, kBlockM);
+    g.tiles_m = ceil_div_i(a.m, PAIR ? 2 * kBlockM : kBlockM);
+    g.sf_row_blocks_a = ceil_div_i(a.m, kBlockM);
     g.tiles_mn = (a.m > 0 && a.n > 0) ? g.tiles_m * ceil_div_i(a.n, BN) : 0;
     g.tiles = g.tiles_mn * (int)a.l;
     g.k_tiles = ceil_div_i(a.k, kBlockK);
     g.k_blocks = ceil_div_i(a.k, kMmaK);
     g.work_tiles = g.k_tiles > 1 ? g.k_tiles : 1;
     g.sf_row_blocks_b = ceil_div_i(a.n, 128);
-    g.sfa_batch = (size_t)g.tiles_m * g.k_blocks * kSfAtomBytes;
+    g.sfa_batch = (size_t)g.sf_row_blocks_a * g.k_blocks * kSfAtomBytes;
     g.sfb_batch = (size_t)g.sf_row_blocks_b * g.k_blocks * kSfAtomBytes;
     g.sfa = static_cast<const uint8_t *>(a.sfa);
     g.sfb = static_cast<const uint8_t *>(a.sfb);
@@ -234,21 +244,36 @@ __device__ __forceinline__ int find_group(const int32_t *prefix, int group_count
     return lo;
 }
 
+// CL: acquire at cluster scope (barriers that threads of the other CTA of a
+// pair arrive on). spin: poll without suspending the thread (barriers that
+// the other CTA completes, whose completion may not wake a suspended
+// waiter at once). On giving up, `peer_abort` (a shared::cluster address, 0
+// for none) is the other CTA's abort flag, set too so that both CTAs of a
+// pair leave their loops.
+template <bool CL = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                             uint64_t timeout_ns, uint32_t *status, uint32_t bit) {
+                                             uint64_t timeout_ns, uint32_t *status, uint32_t bit,
+                                             uint32_t peer_abort = 0, bool spin = false) {
     // Each attempt suspends the thread for at most the bound (capped at
     // 1 ms), and the bound is checked after every failed one.
     const uint32_t hint = timeout_ns < 1000000ull ? (uint32_t)timeout_ns : 1000000u;
-    if (ptx::mbar_try_wait_hint(bar, parity, hint))
+    auto attempt = [&]() {
+        if (spin)
+            return ptx::mbar_test_wait<CL>(bar, parity);
+        return CL ? ptx::mbar_try_wait_hint_cluster(bar, parity, hint) : ptx::mbar_try_wait_hint(bar, parity, hint);
+    };
+    if (attempt())
         return true;
     const uint64_t t0 = ptx::globaltimer();
     while (true) {
-        if (ptx::mbar_try_wait_hint(bar, parity, hint))
+        if (attempt())
             return true;
         if (*abort_flag)
             return false;
         if (ptx::globaltimer() - t0 > timeout_ns) {
             *abort_flag = 1;
+            if (peer_abort)
+                ptx::st_cluster_u32(peer_abort, 1u);
             atomicOr(status, bit);
             return false;
         }
@@ -291,7 +316,7 @@ __device__ __forceinline__ int split_begin(int c, int p, int total_work) {
 // the first split tile), then the rest of its split range (ending, when the
 // range ends inside a tile, with that tile's first piece, which this CTA
 // finishes as its last segment).
-template <int BN, int CAP, bool DEV>
+template <int BN, int CAP, bool DEV, bool PAIR = false>
 struct Cursor {
     // (the kernel parameters are passed to next() by reference rather than
     // kept here: through a stored pointer they would be read with generic
@@ -301,10 +326,11 @@ struct Cursor {
     int tile, tile_end, step;  // whole tiles
     int w, w_end;              // split range [w, w_end) of schedule units
     int phase;                 // 0: head, 1: whole tiles, 2: rest of the split range
+    int rank;                  // CTA pairs: this CTA's rank in its pair (segments carry its own 128-row m-tile)
 
     __device__ __forceinline__ void split_segment(const GemmParams<CAP, DEV> &p, Segment &s, const int limit) {
         s.g = find_group(wprefix, group_count, w);
-        const GInfo gi = group_info<BN>(load_group(p, s.g));
+        const GInfo gi = group_info<BN, PAIR>(load_group(p, s.g));
         const int local = w - wprefix[s.g];
         const int t = local / gi.work_tiles;
         s.ktg = gi.work_tiles;
@@ -313,7 +339,7 @@ struct Cursor {
         s.kt1 = s.kt0 + ((s.ktg - s.kt0) < rest ? (s.ktg - s.kt0) : rest);
         s.b = t / gi.tiles_mn;
         const int tb = t - s.b * gi.tiles_mn;
-        s.tm = tb % gi.tiles_m;
+        s.tm = PAIR ? 2 * (tb % gi.tiles_m) + rank : tb % gi.tiles_m;
         s.tn = tb / gi.tiles_m;
         s.w_tile_end = wprefix[s.g] + (t + 1) * s.ktg;
         w += s.kt1 - s.kt0;
@@ -335,11 +361,11 @@ struct Cursor {
         if (phase == 1) {
             if (tile < tile_end) {
                 s.g = find_group(prefix, group_count, tile);
-                const GInfo gi = group_info<BN>(load_group(p, s.g));
+                const GInfo gi = group_info<BN, PAIR>(load_group(p, s.g));
                 const int t = tile - prefix[s.g];
                 s.b = t / gi.tiles_mn;
                 const int tb = t - s.b * gi.tiles_mn;
-                s.tm = tb % gi.tiles_m;
+                s.tm = PAIR ? 2 * (tb % gi.tiles_m) + rank : tb % gi.tiles_m;
                 s.tn = tb / gi.tiles_m;
                 s.ktg = gi.work_tiles;
                 s.kt0 = 0;
@@ -403,20 +429,30 @@ __device__ __forceinline__ int tile_chunks(const GInfo &gi, const Segment &sg) {
 // whole tile in the main loop, at most kMaxLoopChunks chunks per warp) the
 // warp first moves its chunks from TMEM into registers and arrives on
 // release_bar, so the next tile's MMAs may start, and then stores them; a
-// null `buf` stores each row's 64 bytes straight from registers.
-template <int BN, int CAP, bool DEV>
+// null `buf` stores each row's 64 bytes straight from registers. PAIR:
+// `release_bar` is the shared::cluster address of the accumulator-empty
+// barrier of the pair's even CTA, and a CTA whose 128 rows all lie past m
+// (its half of a pair tile over a short group) only releases.
+template <int BN, int CAP, bool DEV, bool PAIR = false>
 __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, const Segment &sg, const GInfo &gi,
                                               const int kind, const int quarter, const int lane,
                                               const uint32_t t_acc, const int c0, const int c1, uint8_t *buf,
                                               const uint8_t *smem, const int part_stage0, const int pieces,
                                               const uint32_t release_bar = 0) {
-    using C = Cfg<BN, CAP>;
-    if (c0 >= c1) {
-        // no chunks for this warp (a narrow tile), but its release still counts
+    using C = Cfg<BN, CAP, PAIR>;
+    auto release = [&]() {
+        if constexpr (PAIR)
+            ptx::mbar_arrive_cluster(release_bar);
+        else
+            ptx::mbar_arrive(release_bar);
+    };
+    if (c0 >= c1 || sg.tm * kBlockM >= gi.m) {
+        // no chunks for this warp (a narrow tile, or no rows), but its release
+        // still counts
         if (release_bar != 0) {
             __syncwarp();
             if (lane == 0)
-                ptx::mbar_arrive(release_bar);
+                release();
         }
         return;
     }
@@ -553,7 +589,7 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, con
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0)
-            ptx::mbar_arrive(release_bar);
+            release();
 #pragma unroll
         for (int i = 0; i < C::kMaxLoopChunks; ++i) {
             if (c0 + i < c1) {
@@ -584,15 +620,21 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, con
     }
 }
 
-template <int BN, int CAP, bool DEV>
+template <int BN, int CAP, bool DEV, bool PAIR>
 __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams<CAP, DEV> p) {
-    using C = Cfg<BN, CAP>;
+    using C = Cfg<BN, CAP, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t smem_base = ptx::smem_addr(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int group_count = p.group_count;
+    // CTA pairs (clusters of two): this CTA's rank in its pair; the schedule
+    // deals tiles to pairs (slot = pair index), and both CTAs of a pair walk
+    // the same tiles, each its own 128 rows
+    const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+    const int slot = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int nslots = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     // descriptors are patched in this call (host table: only those that changed)
     const bool publish = DEV || p.desc_maps != 0;
     // Tag of this call's partial-tile flags: one more than the last completed
@@ -610,6 +652,11 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     auto sfl_bar = [&](int s) { return bars + 384u + 8u * s; };  // the stage's scale atoms landed
     auto accf_bar = [&](int a) { return bars + 8u * (3 * C::kStages + a); };
     auto acce_bar = [&](int a) { return bars + 8u * (3 * C::kStages + C::kAccStages + a); };
+    // CTA pairs, even CTA: the odd CTA's stage s is ready (A / B landed, its
+    // scales written to its TMEM)
+    auto peer_bar = [&](int s) { return bars + 8u * (3 * C::kStages + 2 * C::kAccStages + s); };
+    // where the epilogue releases accumulator a: the even CTA's barrier in a pair
+    auto acce_release = [&](int a) { return PAIR ? ptx::mapa(acce_bar(a), 0u) : acce_bar(a); };
     const uint32_t drain_bar = bars + 176;    // the MMA thread's issued MMAs have completed
     const uint32_t partial_bar = bars + 184;  // partial tile of a split tile landed in smem
     // Bound of the waits that let this CTA's own asynchronous copies and MMAs
@@ -621,6 +668,11 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     volatile int *s_epi_ok = reinterpret_cast<volatile int *>(bar_area + 208);  // [3]: by segment parity, tail
     volatile uint32_t *s_epoch = reinterpret_cast<volatile uint32_t *>(bar_area + 224);  // this call's epoch
     TailState *s_tail = reinterpret_cast<TailState *>(bar_area + 256);
+    // the other CTA's abort flag (CTA pairs), set with this CTA's
+    const uint32_t peer_abort = PAIR ? ptx::mapa(ptx::smem_addr(bar_area + 196), rank ^ 1u) : 0u;
+    // the odd CTA of a pair: its stage-empty and accumulator-full barriers are
+    // completed by the even CTA's tcgen05 commits
+    const bool remote_commits = PAIR && rank != 0;
     static_assert(256 + sizeof(TailState) <= 384, "barrier area");
     uint8_t *epi_stage = bar_area + C::kBarrierBytes;                // [4 warps][32 rows][64 B]
     int32_t *prefix;
@@ -631,6 +683,13 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     int32_t *wprefix = prefix + (C::kSmemPrefix ? C::kPrefixInts : (int)(cta_prefix_bytes(CAP) / 8));
 
     // ---- set-up -------------------------------------------------------------
+    // CTA pairs: every thread arrives on the cluster barrier (warp 4 once the
+    // mbarriers are initialised) and waits on it before its first access to
+    // the other CTA
+    if constexpr (PAIR) {
+        if (warp != 4 && warp != 5)
+            ptx::cluster_arrive();
+    }
     if (warp == 4) {
         if (lane == 0) {
             for (int s = 0; s < C::kStages; ++s) {
@@ -641,7 +700,11 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             }
             for (int a = 0; a < C::kAccStages; ++a) {
                 ptx::mbar_init(accf_bar(a), 1);
-                ptx::mbar_init(acce_bar(a), 8);
+                ptx::mbar_init(acce_bar(a), PAIR ? 16 : 8);  // the epilogue warps of both CTAs of a pair
+            }
+            if constexpr (PAIR) {
+                for (int s = 0; s < C::kStages; ++s)
+                    ptx::mbar_init(peer_bar(s), 1);
             }
             ptx::mbar_init(partial_bar, 1);
             ptx::mbar_init(drain_bar, 1);
@@ -652,6 +715,10 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             s_tail->part_stage0 = 0;
             s_tail->pieces = 0;
             ptx::fence_mbar_init();
+        }
+        if constexpr (PAIR) {
+            __syncwarp();
+            ptx::cluster_arrive();
         }
         // Patch the descriptors of this CTA's share of the groups.
         uint32_t patched = 0;
@@ -707,9 +774,16 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
         __syncwarp();
         ptx::named_barrier(2, 96);
         ptx::named_barrier_arrive(3, C::kThreads);
+        if constexpr (PAIR)
+            ptx::cluster_wait();
     } else if (warp == 5) {
-        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::kTmemCols);
-        ptx::tmem_relinquish();
+        // a pair's allocation is made by this warp of both CTAs together
+        if constexpr (PAIR) {
+            ptx::cluster_arrive();
+            ptx::cluster_wait();
+        }
+        ptx::tmem_alloc<C::kCtaGroup>(ptx::smem_addr(tmem_slot), C::kTmemCols);
+        ptx::tmem_relinquish<C::kCtaGroup>();
     } else if (warp == 7) {
         // This call's epoch, for the producer, the partial-tile flags and the
         // counter reset (read before the producer counts this CTA as done).
@@ -731,7 +805,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                 long long t = 0, w = 0;
                 if (g < group_count) {
                     const GroupArgs a = load_group(p, g, &bad);
-                    t = (a.m > 0 && a.n > 0) ? (long long)ceil_div_i(a.m, kBlockM) * ceil_div_i(a.n, BN) * a.l : 0;
+                    t = (a.m > 0 && a.n > 0) ? (long long)ceil_div_i(a.m, C::kTileM) * ceil_div_i(a.n, BN) * a.l : 0;
                     const int kt = ceil_div_i(a.k, kBlockK);
                     w = t * (kt > 1 ? kt : 1);
                 }
@@ -772,7 +846,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
 #pragma unroll 4
             for (int g = 0; g < group_count; ++g) {
                 const GroupArgs &a = p.groups[g];
-                const int tiles = (a.m > 0 && a.n > 0) ? ceil_div_i(a.m, kBlockM) * ceil_div_i(a.n, BN) * a.l : 0;
+                const int tiles = (a.m > 0 && a.n > 0) ? ceil_div_i(a.m, C::kTileM) * ceil_div_i(a.n, BN) * a.l : 0;
                 const int kt = ceil_div_i(a.k, kBlockK);
                 if (lane == (g & 31)) {
                     prefix[g] = bt;
@@ -791,6 +865,10 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     }
     uint32_t tmem_base = 0;  // warp 4 reads it after the role loops
     if (warp != 4) {
+        if constexpr (PAIR) {
+            if (warp != 5)
+                ptx::cluster_wait();
+        }
         ptx::tc_fence_before();
         ptx::named_barrier(3, C::kThreads);
         ptx::tc_fence_after();
@@ -806,10 +884,11 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     const int total_work = DEV ? wprefix[group_count] : p.total_work;
     int split_tile = p.split_tile;
     if constexpr (DEV)
-        split_tile = choose_split_tile(total_tiles, (int)gridDim.x,
-                                       p.ws.partial_slots >= (int)gridDim.x ? p.split : 0);
+        split_tile = choose_split_tile(total_tiles, nslots, p.ws.partial_slots >= nslots ? p.split : 0);
+    if constexpr (PAIR)
+        split_tile = total_tiles;  // pairs run whole tiles only
     const int split = split_tile < total_tiles ? 1 : 0;
-    const int P = (split && split_tile == 0 && total_work < (int)gridDim.x) ? total_work : (int)gridDim.x;
+    const int P = (split && split_tile == 0 && total_work < nslots) ? total_work : nslots;
     const int sk0 = split_tile == 0 ? 0
                                     : tile_first_unit<BN>(p, prefix, wprefix, group_count, split_tile, total_tiles,
                                                           total_work);
@@ -819,12 +898,12 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     const int Psk = split ? (total_work - sk0 < P ? total_work - sk0 : P) : 0;
     // first schedule unit of CTA c's part of the split range
     auto sk_begin = [&](int c) { return sk0 + split_begin(c, Psk, total_work - sk0); };
-    Cursor<BN, CAP, DEV> cursor0{prefix, wprefix, group_count, (int)blockIdx.x, split_tile, P, 0, 0, 0};
-    if (split && (int)blockIdx.x < Psk) {
-        cursor0.w = sk_begin(blockIdx.x);
-        cursor0.w_end = sk_begin(blockIdx.x + 1);
+    Cursor<BN, CAP, DEV, PAIR> cursor0{prefix, wprefix, group_count, slot, split_tile, P, 0, 0, 0, (int)rank};
+    if (split && slot < Psk) {
+        cursor0.w = sk_begin(slot);
+        cursor0.w_end = sk_begin(slot + 1);
     }
-    if ((int)blockIdx.x >= P)
+    if (slot >= P)
         cursor0.tile = cursor0.tile_end;  // no whole tiles either
 
     if (warp == 4) {
@@ -853,12 +932,12 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                     *p.ws.epoch = *s_epoch;
                 }
             };
-            Cursor<BN, CAP, DEV> cur = cursor0;
+            auto cur = cursor0;
             Segment sg;
             bool any = false;
             while (ok && cur.next(p, sg)) {
                 any = true;
-                const GInfo gi = group_info<BN>(load_group(p, sg.g));
+                const GInfo gi = group_info<BN, PAIR>(load_group(p, sg.g));
                 const int k_tiles = gi.k_tiles;
                 const int kend = sg.kt1 < k_tiles ? sg.kt1 : k_tiles;
                 if (sg.kt0 >= kend)
@@ -876,14 +955,18 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                         ptx::tmap_acquire(tmap_sfb);
                     prev_g = sg.g;
                 }
+                // a CTA of a pair whose 128 rows all lie past m loads no A and
+                // no A scales (its accumulator rows are never stored)
+                const bool a_live = !PAIR || sg.tm * kBlockM < gi.m;
                 const uint8_t *sfa = gi.sfa + (size_t)sg.b * gi.sfa_batch + (size_t)sg.tm * k_blocks * kSfAtomBytes;
                 int sfb_blocks = gi.sf_row_blocks_b - sg.tn * C::kSfbRowBlocks;
                 sfb_blocks = sfb_blocks < C::kSfbRowBlocks ? sfb_blocks : C::kSfbRowBlocks;
                 const uint8_t *sfb =
                     gi.sfb + (size_t)sg.b * gi.sfb_batch + (size_t)sg.tn * C::kSfbRowBlocks * k_blocks * kSfAtomBytes;
                 for (int kt = sg.kt0; kt < kend; ++kt) {
+                    // (the odd CTA of a pair is released by the even CTA's commits)
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns, p.ws.status,
-                                      kStatusProducerTimeout)) {
+                                      kStatusProducerTimeout, peer_abort, remote_commits)) {
                         ok = false;
                         break;
                     }
@@ -901,9 +984,10 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                         // row block reads the next rows, which only reach
                         // accumulator columns >= n): one copy operation fewer
                         // per stage, which the ring's round trip pays for
-                        ptx::mbar_arrive_expect_tx(sb, sf_bytes + C::kSfbBytes);
-                        ptx::bulk_load(st + C::kABytes + C::kBBytes, sfa + (size_t)(4 * kt) * kSfAtomBytes, sf_bytes,
-                                       sb, pol_a);
+                        ptx::mbar_arrive_expect_tx(sb, (a_live ? sf_bytes : 0u) + C::kSfbBytes);
+                        if (a_live)
+                            ptx::bulk_load(st + C::kABytes + C::kBBytes, sfa + (size_t)(4 * kt) * kSfAtomBytes,
+                                           sf_bytes, sb, pol_a);
                         ptx::tma_load_2d(st + C::kABytes + C::kBBytes + C::kSfaBytes, tmap_sfb,
                                          kt * (4 * kSfAtomBytes / 8), sg.b * gi.sf_row_blocks_b + sg.tn * 2, sb,
                                          pol_b);
@@ -915,12 +999,15 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                             ptx::bulk_load(st + C::kABytes + C::kBBytes + C::kSfaBytes + j * 4 * kSfAtomBytes,
                                            sfb + ((size_t)j * k_blocks + 4 * kt) * kSfAtomBytes, sf_bytes, sb, pol_b);
                     }
-                    ptx::mbar_arrive_expect_tx(fb, C::kABytes + C::kBBytes);
+                    ptx::mbar_arrive_expect_tx(fb, (a_live ? (uint32_t)C::kABytes : 0u) + C::kBBytes);
                     // batch b's rows start at b * m (b * n) of the group's stack;
                     // rows a tile reads past its batch only reach accumulator
-                    // rows / columns that the epilogue does not store
-                    ptx::tma_load_2d(st, tmap_a, kt * 128, sg.b * gi.m + sg.tm * kBlockM, fb, pol_a);
-                    ptx::tma_load_2d(st + C::kABytes, tmap_b, kt * 128, sg.b * gi.n + sg.tn * BN, fb, pol_b);
+                    // rows / columns that the epilogue does not store. A CTA of
+                    // a pair loads its half of the tile's B rows.
+                    if (a_live)
+                        ptx::tma_load_2d(st, tmap_a, kt * 128, sg.b * gi.m + sg.tm * kBlockM, fb, pol_a);
+                    ptx::tma_load_2d(st + C::kABytes, tmap_b, kt * 128,
+                                     sg.b * gi.n + sg.tn * BN + (int)rank * C::kBRows, fb, pol_b);
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::kStages) {
@@ -962,7 +1049,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                 s_tail->pieces = pieces;
                 if (flags_ok) {
                     ptx::fence_proxy_async_global();
-                    const int nch = tile_chunks<BN>(group_info<BN>(load_group(p, sg.g)), sg);
+                    const int nch = tile_chunks<BN>(group_info<BN, PAIR>(load_group(p, sg.g)), sg);
                     const char *src =
                         reinterpret_cast<const char *>(p.ws.partials) + (size_t)(cta + 1) * kPartialSlotBytes;
                     bool good = true;
@@ -972,7 +1059,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                         const int s = (stage + cc / C::kPartialChunksPerStage) % C::kStages;
                         if (((armed >> s) & 1u) &&
                             !wait_bounded(empty_bar(s), (armed_parity >> s) & 1u, abort_flag, p.timeout_ns,
-                                          p.ws.status, kStatusProducerTimeout)) {
+                                          p.ws.status, kStatusProducerTimeout, peer_abort)) {
                             good = false;
                             break;
                         }
@@ -1002,28 +1089,61 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             }
         }
     } else if (warp == 5) {
-        // ===================== MMA issuer =====================
-        if (lane == 0) {
+        if (PAIR && rank != 0) {
+            // ============ relay (odd CTA of a pair) ============
+            // Tells the even CTA's MMA thread when this CTA's stage is ready:
+            // its A / B tiles have landed and its scale writers are done.
+            if (lane == 0) {
+                int stage = 0;
+                uint32_t phase = 0;
+                bool ok = true;
+                auto cur = cursor0;
+                Segment sg;
+                while (ok && cur.next(p, sg)) {
+                    const GInfo gi = group_info<BN, PAIR>(load_group(p, sg.g));
+                    const int kend = sg.kt1 < gi.k_tiles ? sg.kt1 : gi.k_tiles;
+                    for (int kt = sg.kt0; kt < kend; ++kt) {
+                        if (!wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status,
+                                                kStatusMmaTimeout, peer_abort) ||
+                            !wait_bounded(sff_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status,
+                                                kStatusMmaTimeout, peer_abort)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::mbar_arrive_cluster(ptx::mapa(peer_bar(stage), 0u));
+                        if (++stage == C::kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+        } else if (lane == 0) {
+            // ===================== MMA issuer =====================
+            // (CTA pairs: the even CTA issues the pair's MMAs and commits to
+            // both CTAs' barriers)
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            Cursor<BN, CAP, DEV> cur = cursor0;
+            auto cur = cursor0;
             Segment sg;
             while (ok && cur.next(p, sg)) {
-                const GInfo gi = group_info<BN>(load_group(p, sg.g));
+                const GInfo gi = group_info<BN, PAIR>(load_group(p, sg.g));
                 const int k_tiles = gi.k_tiles;
                 const int k_blocks = gi.k_blocks;
                 const int kend = sg.kt1 < k_tiles ? sg.kt1 : k_tiles;
-                if (!wait_bounded(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns, p.ws.status,
-                                  kStatusMmaTimeout))
+                if (!wait_bounded<PAIR>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.timeout_ns, p.ws.status,
+                                        kStatusMmaTimeout, peer_abort, PAIR))
                     break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::kAccCols);
                 for (int kt = sg.kt0; kt < kend; ++kt) {
                     if (!wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status,
-                                      kStatusMmaTimeout) ||
+                                            kStatusMmaTimeout, peer_abort) ||
                         !wait_bounded(sff_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status,
-                                      kStatusMmaTimeout)) {
+                                            kStatusMmaTimeout, peer_abort) ||
+                        (PAIR && !wait_bounded<true>(peer_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status,
+                                                     kStatusMmaTimeout, peer_abort, true))) {
                         ok = false;
                         break;
                     }
@@ -1036,10 +1156,13 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                     const uint64_t bdesc = ptx::sdesc_kmajor_sw128(st + C::kABytes);
                     for (int kb = 0; kb < nkb; ++kb) {
                         // +32 bytes per 64-element k-block inside the swizzled row
-                        ptx::tc_mma_mxf4nvf4(d_tmem, adesc + 2u * kb, bdesc + 2u * kb, C::kIdesc, sfa_t + 4 * kb,
-                                             sfb_t + kb * (BN / 32), (kt != sg.kt0 || kb != 0) ? 1u : 0u);
+                        ptx::tc_mma_mxf4nvf4<C::kCtaGroup>(d_tmem, adesc + 2u * kb, bdesc + 2u * kb, C::kIdesc,
+                                                           sfa_t + 4 * kb, sfb_t + kb * (BN / 32),
+                                                           (kt != sg.kt0 || kb != 0) ? 1u : 0u);
                     }
-                    ptx::tc_commit(empty_bar(stage));
+                    ptx::tc_commit<C::kCtaGroup>(empty_bar(stage));
+                    if constexpr (PAIR)
+                        ptx::tc_commit<C::kCtaGroup>(ptx::mapa(empty_bar(stage), 1u));
                     if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -1047,7 +1170,9 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                 }
                 if (!ok)
                     break;
-                ptx::tc_commit(accf_bar(acc));
+                ptx::tc_commit<C::kCtaGroup>(accf_bar(acc));
+                if constexpr (PAIR)
+                    ptx::tc_commit<C::kCtaGroup>(ptx::mapa(accf_bar(acc), 1u));
                 if (++acc == C::kAccStages) {
                     acc = 0;
                     acc_phase ^= 1u;
@@ -1056,7 +1181,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             // Every MMA this thread issued completes before the CTA can free
             // TMEM -- on the normal path the epilogue already waits for them,
             // after an abort nothing else would.
-            ptx::tc_commit(drain_bar);
+            ptx::tc_commit<C::kCtaGroup>(drain_bar);
             const uint64_t t0 = ptx::globaltimer();
             while (!ptx::mbar_try_wait(drain_bar, 0) && ptx::globaltimer() - t0 < drain_ns) {
             }
@@ -1069,17 +1194,17 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        Cursor<BN, CAP, DEV> cur = cursor0;
+        auto cur = cursor0;
         Segment sg;
         while (ok && cur.next(p, sg)) {
-            const GInfo gi = group_info<BN>(load_group(p, sg.g));
+            const GInfo gi = group_info<BN, PAIR>(load_group(p, sg.g));
             const int k_tiles = gi.k_tiles;
             const int k_blocks = gi.k_blocks;
             const int kend = sg.kt1 < k_tiles ? sg.kt1 : k_tiles;
             for (int kt = sg.kt0; kt < kend; ++kt) {
                 int got = 0;
                 if (lane == 0)
-                    got = wait_bounded(sfl_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status, kStatusMmaTimeout)
+                    got = wait_bounded(sfl_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status, kStatusMmaTimeout, peer_abort)
                               ? 1
                               : 0;
                 got = __shfl_sync(0xffffffffu, got, 0);
@@ -1147,21 +1272,21 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
         int acc = 0, it = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        Cursor<BN, CAP, DEV> cur = cursor0;
+        auto cur = cursor0;
         Segment sg;
         const bool have = cur.next(p, sg);
         while (have) {
             Segment nx;
             if (!cur.next(p, nx))
                 break;
-            const GInfo gi = group_info<BN>(load_group(p, sg.g));
+            const GInfo gi = group_info<BN, PAIR>(load_group(p, sg.g));
             // a first piece of a split tile is always a CTA's last segment
             const int kind = sg.kt0 > 0 ? kEpiCont : kEpiWhole;
             // One thread waits for the accumulator; the eight warps leave or
             // stay together (the TMEM loads are warp-collective).
             if (threadIdx.x == 0)
                 s_epi_ok[it & 1] = wait_bounded(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns, p.ws.status,
-                                                kStatusEpilogueTimeout)
+                                                kStatusEpilogueTimeout, peer_abort, remote_commits)
                                        ? 1
                                        : 0;
             ptx::named_barrier(4, 256);
@@ -1175,14 +1300,18 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             // a whole tile releases the accumulator once its chunks are in
             // registers; a partial tile (fp32) goes out chunk by chunk first
             const uint32_t t_acc = tmem_base + (uint32_t)(acc * C::kAccCols);
-            epilogue_warp<BN, CAP, DEV>(p, sg, gi, kind, quarter, lane, t_acc, first_half ? 0 : half,
+            epilogue_warp<BN, CAP, DEV, PAIR>(p, sg, gi, kind, quarter, lane, t_acc, first_half ? 0 : half,
                                    first_half ? half : nch, first_half ? epi_stage + warp * C::kEpiStageBytes : nullptr,
-                                   smem, 0, 0, kind == kEpiWhole ? acce_bar(acc) : 0u);
+                                   smem, 0, 0, kind == kEpiWhole ? acce_release(acc) : 0u);
             if (kind != kEpiWhole) {
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
-                    ptx::mbar_arrive(acce_bar(acc));
+                if (lane == 0) {
+                    if constexpr (PAIR)
+                        ptx::mbar_arrive_cluster(acce_release(acc));
+                    else
+                        ptx::mbar_arrive(acce_bar(acc));
+                }
             }
             if (kind == kEpiCont) {
                 // publish this CTA's partial tile
@@ -1218,11 +1347,11 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     if (warp < 8) {
         const TailState ts = *s_tail;
         const Segment sg = ts.seg;
-        const GInfo gi = group_info<BN>(load_group(p, ts.valid ? sg.g : 0));
+        const GInfo gi = group_info<BN, PAIR>(load_group(p, ts.valid ? sg.g : 0));
         const int kind = sg.kt0 > 0 ? kEpiCont : ((split && sg.kt1 < sg.ktg) ? kEpiFinish : kEpiWhole);
         if (threadIdx.x == 0) {
             int ok = ts.valid && wait_bounded(accf_bar(ts.acc), (uint32_t)ts.acc_phase, abort_flag, p.timeout_ns,
-                                              p.ws.status, kStatusEpilogueTimeout);
+                                              p.ws.status, kStatusEpilogueTimeout, peer_abort, remote_commits);
             if (ts.part_state) {
                 // the partial-tile copies must land before the CTA exits, even
                 // after an abort
@@ -1250,7 +1379,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             const int quarter = warp & 3;
             uint8_t *buf = warp < 4 ? epi_stage + warp * C::kEpiStageBytes
                                     : smem + (warp - 4) * C::kStageBytes + C::kStageBytes - C::kEpiStageBytes;
-            epilogue_warp<BN, CAP, DEV>(p, sg, gi, kind, quarter, lane, tmem_base + (uint32_t)(ts.acc * C::kAccCols),
+            epilogue_warp<BN, CAP, DEV, PAIR>(p, sg, gi, kind, quarter, lane, tmem_base + (uint32_t)(ts.acc * C::kAccCols),
                                    warp < 4 ? 0 : half, warp < 4 ? half : nch, buf, smem, ts.part_stage0,
                                    ts.pieces);
             if (kind == kEpiCont) {
@@ -1264,15 +1393,21 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     }
 
     // ---- teardown ----------------------------------------------------------
+    // CTA pairs: neither CTA leaves (or frees the pair's TMEM, which both free
+    // together) while the other may still touch its shared memory or TMEM
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) {
+        ptx::cluster_arrive();
+        ptx::cluster_wait();
+    }
     if (warp == 5) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+        ptx::tmem_dealloc<C::kCtaGroup>(tmem_base, C::kTmemCols);
     }
 }
 
-template <int BN, int CAP, bool DEV>
+template <int BN, int CAP, bool DEV, bool PAIR = false>
 cudaError_t launch_cap(const GemmLaunch &cfg, const GroupArgs *groups, const WorkspaceView &ws,
                        const void *tmpl_a, const void *tmpl_b, const void *tmpl_sfb, cudaStream_t stream) {
     static_assert(sizeof(GemmParams<CAP, DEV>) <= 32000, "kernel parameter limit");
@@ -1300,37 +1435,67 @@ cudaError_t launch_cap(const GemmLaunch &cfg, const GroupArgs *groups, const Wor
     }
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)cfg.grid, 1, 1);
-    lc.blockDim = dim3(Cfg<BN, CAP>::kThreads, 1, 1);
-    lc.dynamicSmemBytes = Cfg<BN, CAP>::kSmemBytes;
+    lc.blockDim = dim3(Cfg<BN, CAP, PAIR>::kThreads, 1, 1);
+    lc.dynamicSmemBytes = Cfg<BN, CAP, PAIR>::kSmemBytes;
     lc.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     lc.attrs = attr;
-    lc.numAttrs = 1;
-    return cudaLaunchKernelEx(&lc, grouped_gemm_kernel<BN, CAP, DEV>, prm);
+    lc.numAttrs = PAIR ? 2 : 1;
+    return cudaLaunchKernelEx(&lc, grouped_gemm_kernel<BN, CAP, DEV, PAIR>, prm);
 }
 
 }  // namespace
 
 cudaError_t prepare_gemm_kernels(int /*device*/) {
     cudaError_t e = cudaSuccess;
-#define NVFP4_SET_SMEM(BN, CAP, DEV)                                                                             \
-    if (e == cudaSuccess)                                                                                        \
-        e = cudaFuncSetAttribute(grouped_gemm_kernel<BN, CAP, DEV>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                 (int)Cfg<BN, CAP>::kSmemBytes);
-    NVFP4_SET_SMEM(128, kSmallGroups, false)
-    NVFP4_SET_SMEM(128, kMediumGroups, false)
-    NVFP4_SET_SMEM(128, NVFP4_MAX_GROUPS, false)
-    NVFP4_SET_SMEM(256, kSmallGroups, false)
-    NVFP4_SET_SMEM(256, kMediumGroups, false)
-    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS, false)
-    NVFP4_SET_SMEM(128, kMediumGroups, true)
-    NVFP4_SET_SMEM(128, NVFP4_MAX_GROUPS, true)
-    NVFP4_SET_SMEM(256, kMediumGroups, true)
-    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS, true)
+#define NVFP4_SET_SMEM(BN, CAP, DEV, PAIR)                                                          \
+    if (e == cudaSuccess)                                                                           \
+        e = cudaFuncSetAttribute(grouped_gemm_kernel<BN, CAP, DEV, PAIR>,                           \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN, CAP, PAIR>::kSmemBytes);
+    NVFP4_SET_SMEM(128, kSmallGroups, false, false)
+    NVFP4_SET_SMEM(128, kMediumGroups, false, false)
+    NVFP4_SET_SMEM(128, NVFP4_MAX_GROUPS, false, false)
+    NVFP4_SET_SMEM(256, kSmallGroups, false, false)
+    NVFP4_SET_SMEM(256, kMediumGroups, false, false)
+    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS, false, false)
+    NVFP4_SET_SMEM(128, kMediumGroups, true, false)
+    NVFP4_SET_SMEM(128, NVFP4_MAX_GROUPS, true, false)
+    NVFP4_SET_SMEM(256, kMediumGroups, true, false)
+    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS, true, false)
+    NVFP4_SET_SMEM(256, kSmallGroups, false, true)
+    NVFP4_SET_SMEM(256, kMediumGroups, false, true)
+    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS, false, true)
 #undef NVFP4_SET_SMEM
     return e;
+}
+
+int pair_capacity(int /*device*/) {
+    // The pair instantiation with the most shared memory (group table prefix
+    // sums in shared memory) bounds how many pairs are resident at once.
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(2, 1, 1);
+    lc.blockDim = dim3(Cfg<256, kMediumGroups, true>::kThreads, 1, 1);
+    lc.dynamicSmemBytes = Cfg<256, kMediumGroups, true>::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, (void *)grouped_gemm_kernel<256, kMediumGroups, false, true>, &lc) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return clusters;
 }
 
 cudaError_t launch_grouped(const GemmLaunch &cfg, const GroupArgs *groups, const WorkspaceView &ws,
@@ -1342,6 +1507,15 @@ cudaError_t launch_grouped(const GemmLaunch &cfg, const GroupArgs *groups, const
     if (cfg.group_count > kMediumGroups && ws.prefix_slots < cfg.grid)
         return cudaErrorInvalidValue;
     const bool wide = cfg.block_n == 256;
+    if (cfg.pair) {
+        if (!wide || cfg.device_table || cfg.split || (cfg.grid & 1))
+            return cudaErrorInvalidValue;
+        if (cfg.group_count <= kSmallGroups)
+            return launch_cap<256, kSmallGroups, false, true>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream);
+        if (cfg.group_count <= kMediumGroups)
+            return launch_cap<256, kMediumGroups, false, true>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream);
+        return launch_cap<256, NVFP4_MAX_GROUPS, false, true>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream);
+    }
     if (cfg.device_table) {
         // shared-memory prefix sums up to kMediumGroups groups
         if (cfg.group_count <= kMediumGroups)
