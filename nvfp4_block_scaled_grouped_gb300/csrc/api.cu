@@ -249,11 +249,15 @@ int split_override() {
     return -1;
 }
 
-// NVFP4_PAIR=1 selects the CTA-pair kernel for calls that run whole tiles.
+// NVFP4_PAIR selects a cluster kernel for calls that run whole tiles: 1 the
+// CTA pair (cta_group::2 MMAs), 2 the multicast cluster, 0 neither; unset:
+// the library's choice.
 int pair_override() {
     const char *s = std::getenv("NVFP4_PAIR");
-    if (s && *s)
-        return std::atoi(s) == 1 ? 1 : 0;
+    if (s && *s) {
+        const int v = std::atoi(s);
+        return v == 1 || v == 2 ? v : 0;
+    }
     return -1;
 }
 
@@ -313,11 +317,13 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
             cfg.grid = (int)(total_work < sms ? total_work : sms);
         else
             cfg.grid = sms;  // whole waves use every SM
-        // CTA pairs (256 x 256 tiles, whole tiles only): only when forced
-        // with NVFP4_PAIR=1, and not with a split schedule forced.
+        // Clusters of two (256 x 256 tiles, whole tiles only): when selected
+        // with NVFP4_PAIR, and not with a split schedule forced.
         const int pmode = pair_override();
-        cfg.pair = block_n == 256 && st->pairs > 0 && pmode == 1 && pair_work <= 0x7fffffffLL && forced <= 0;
-        if (cfg.pair) {
+        cfg.cluster = (block_n == 256 && st->pairs > 0 && pmode > 0 && pair_work <= 0x7fffffffLL && forced <= 0)
+                          ? pmode
+                          : 0;
+        if (cfg.cluster) {
             cfg.split = 0;
             cfg.split_tile = (int)pair_tiles;
             cfg.grid = 2 * (int)(pair_tiles < st->pairs ? pair_tiles : st->pairs);
@@ -328,7 +334,7 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
             return fail(NVFP4_ERR_UNSUPPORTED, "workspace has %d CTA slots, the launch needs %d", prefix_slots,
                         cfg.grid);
         // rows of B per TMA box: a CTA of a pair loads half of a 256-row tile
-        b_box = cfg.pair ? 128 : block_n;
+        b_box = cfg.cluster == 1 ? 128 : block_n;
         // Descriptors to patch: those whose region-0 slot does not already
         // hold this group's pointer and shape (region 0 is written only by
         // this workspace's eager calls, in stream order). A captured launch
@@ -413,7 +419,7 @@ int launch_device_table(int group_count, const DeviceTable &dt, int block_n, voi
     cfg.capacity = capacity;
     cfg.timeout_ns = watchdog_ns();
     cfg.device_table = true;
-    cfg.pair = false;
+    cfg.cluster = 0;
     cfg.dt = dt;
     (void)state;  // region 0 and its host cache are left alone
     const WorkspaceView ws = second_region(workspace_view(ws_base, capacity, slots, slots, 2));

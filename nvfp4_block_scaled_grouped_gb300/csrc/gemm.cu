@@ -81,16 +81,28 @@ namespace {
 
 constexpr int kPartialChunkBytes = 8 * kBlockM * 16;  // one 32-column chunk of an fp32 partial tile
 
-// PAIR: a cluster of two CTAs computes 256 x BN tiles with cta_group::2 MMAs
-// (M = 256): each CTA stages its own 128 rows of A and its half (BN / 2 rows)
-// of B, and holds its 128 rows of the accumulator.
-template <int BN, int CAP, bool PAIR = false>
+// CLU: how CTAs cooperate on a tile.
+//   0  one CTA per 128 x BN tile.
+//   1  CTA pair: a cluster of two CTAs computes 256 x BN tiles with
+//      cta_group::2 MMAs (M = 256) issued by the even CTA: each CTA stages its
+//      own 128 rows of A and its half (BN / 2 rows) of B, and holds its 128
+//      rows of the accumulator.
+//   2  multicast cluster: a cluster of two CTAs computes the two 128 x BN
+//      tiles of a 256 x BN block, each with its own cta_group::1 MMAs; the
+//      B tile and its scales, which both need, are fetched once per cluster
+//      by TMA multicast into both CTAs (B by the even CTA, the B scales by the
+//      odd one), so each CTA issues three copies per k-tile instead of four.
+template <int BN, int CAP, int CLU = 0>
 struct Cfg {
     static_assert(BN == 128 || BN == 256, "BLOCK_N");
-    static_assert(!PAIR || BN == 256, "CTA pairs use 256-column tiles");
-    static constexpr int kTileM = PAIR ? 2 * kBlockM : kBlockM;    // rows of C per schedule tile
-    static constexpr int kBRows = PAIR ? BN / 2 : BN;              // rows of B this CTA stages
-    static constexpr int kStages = PAIR ? 5 : ((BN == 128) ? 6 : 4);
+    static_assert(CLU >= 0 && CLU <= 2, "cluster mode");
+    static_assert(CLU == 0 || BN == 256, "clusters use 256-column tiles");
+    static constexpr bool kCluster = CLU != 0;
+    static constexpr bool kPairMma = CLU == 1;
+    static constexpr bool kMcast = CLU == 2;
+    static constexpr int kTileM = kCluster ? 2 * kBlockM : kBlockM;  // rows of C per schedule tile
+    static constexpr int kBRows = kPairMma ? BN / 2 : BN;            // rows of B in this CTA's stage
+    static constexpr int kStages = kPairMma ? 5 : ((BN == 128) ? 6 : 4);
     static constexpr int kAccStages = (BN == 128) ? 2 : 1;
     static constexpr int kABytes = kBlockM * 128;                  // 128 rows x 256 fp4
     static constexpr int kBBytes = kBRows * 128;                   // kBRows rows x 256 fp4
@@ -114,7 +126,7 @@ struct Cfg {
     // accumulator barriers from 0, scratch from 176, scales-landed per stage
     // from 384
     static constexpr int kBarrierBytes = 448;
-    static_assert(((PAIR ? 4 : 3) * kStages + 2 * kAccStages) * 8 <= 176 && kStages <= 8, "barrier area");
+    static_assert(((kPairMma ? 4 : 3) * kStages + 2 * kAccStages) * 8 <= 176 && kStages <= 8, "barrier area");
     static constexpr int kEpiStageBytes = 32 * 64;                 // per epilogue warp: 32 rows x 32 fp16
     // A finishing CTA receives the next piece's partial tile in ring stages,
     // kPartialChunksPerStage 16 KiB chunks (32 columns x 128 rows fp32) per
@@ -129,8 +141,8 @@ struct Cfg {
     static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kBarrierBytes + 4 * kEpiStageBytes +
                                          (kSmemPrefix ? 2 * sizeof(int32_t) * kPrefixInts : 0);
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    static constexpr uint32_t kIdesc = ptx::idesc_mxf4nvf4(kTileM, BN);
-    static constexpr int kCtaGroup = PAIR ? 2 : 1;
+    static constexpr uint32_t kIdesc = ptx::idesc_mxf4nvf4(kPairMma ? 2 * kBlockM : kBlockM, BN);
+    static constexpr int kCtaGroup = kPairMma ? 2 : 1;
 };
 
 // DEV: the group table is the caller's device arrays (`dt`), else `groups`.
@@ -208,14 +220,15 @@ struct GInfo {
     void *c;
 };
 
-template <int BN, bool PAIR = false>
+// CLUSTER: schedule tiles of 256 rows (clusters of two CTAs).
+template <int BN, bool CLUSTER = false>
 __device__ __forceinline__ GInfo group_info(const GroupArgs &a) {
     GInfo g;
     g.m = a.m;
     g.n = a.n;
     g.k = a.k;
     g.l = a.l;
-    g.tiles_m = ceil_div_i(a.m, PAIR ? 2 * kBlockM : kBlockM);
+    g.tiles_m = ceil_div_i(a.m, CLUSTER ? 2 * kBlockM : kBlockM);
     g.sf_row_blocks_a = ceil_div_i(a.m, kBlockM);
     g.tiles_mn = (a.m > 0 && a.n > 0) ? g.tiles_m * ceil_div_i(a.n, BN) : 0;
     g.tiles = g.tiles_mn * (int)a.l;
@@ -316,7 +329,7 @@ __device__ __forceinline__ int split_begin(int c, int p, int total_work) {
 // the first split tile), then the rest of its split range (ending, when the
 // range ends inside a tile, with that tile's first piece, which this CTA
 // finishes as its last segment).
-template <int BN, int CAP, bool DEV, bool PAIR = false>
+template <int BN, int CAP, bool DEV, bool CLUSTER = false>
 struct Cursor {
     // (the kernel parameters are passed to next() by reference rather than
     // kept here: through a stored pointer they would be read with generic
@@ -326,11 +339,11 @@ struct Cursor {
     int tile, tile_end, step;  // whole tiles
     int w, w_end;              // split range [w, w_end) of schedule units
     int phase;                 // 0: head, 1: whole tiles, 2: rest of the split range
-    int rank;                  // CTA pairs: this CTA's rank in its pair (segments carry its own 128-row m-tile)
+    int rank;                  // clusters: this CTA's rank in its cluster (segments carry its own 128-row m-tile)
 
     __device__ __forceinline__ void split_segment(const GemmParams<CAP, DEV> &p, Segment &s, const int limit) {
         s.g = find_group(wprefix, group_count, w);
-        const GInfo gi = group_info<BN, PAIR>(load_group(p, s.g));
+        const GInfo gi = group_info<BN, CLUSTER>(load_group(p, s.g));
         const int local = w - wprefix[s.g];
         const int t = local / gi.work_tiles;
         s.ktg = gi.work_tiles;
@@ -339,7 +352,7 @@ struct Cursor {
         s.kt1 = s.kt0 + ((s.ktg - s.kt0) < rest ? (s.ktg - s.kt0) : rest);
         s.b = t / gi.tiles_mn;
         const int tb = t - s.b * gi.tiles_mn;
-        s.tm = PAIR ? 2 * (tb % gi.tiles_m) + rank : tb % gi.tiles_m;
+        s.tm = CLUSTER ? 2 * (tb % gi.tiles_m) + rank : tb % gi.tiles_m;
         s.tn = tb / gi.tiles_m;
         s.w_tile_end = wprefix[s.g] + (t + 1) * s.ktg;
         w += s.kt1 - s.kt0;
@@ -361,11 +374,11 @@ struct Cursor {
         if (phase == 1) {
             if (tile < tile_end) {
                 s.g = find_group(prefix, group_count, tile);
-                const GInfo gi = group_info<BN, PAIR>(load_group(p, s.g));
+                const GInfo gi = group_info<BN, CLUSTER>(load_group(p, s.g));
                 const int t = tile - prefix[s.g];
                 s.b = t / gi.tiles_mn;
                 const int tb = t - s.b * gi.tiles_mn;
-                s.tm = PAIR ? 2 * (tb % gi.tiles_m) + rank : tb % gi.tiles_m;
+                s.tm = CLUSTER ? 2 * (tb % gi.tiles_m) + rank : tb % gi.tiles_m;
                 s.tn = tb / gi.tiles_m;
                 s.ktg = gi.work_tiles;
                 s.kt0 = 0;
@@ -429,19 +442,20 @@ __device__ __forceinline__ int tile_chunks(const GInfo &gi, const Segment &sg) {
 // whole tile in the main loop, at most kMaxLoopChunks chunks per warp) the
 // warp first moves its chunks from TMEM into registers and arrives on
 // release_bar, so the next tile's MMAs may start, and then stores them; a
-// null `buf` stores each row's 64 bytes straight from registers. PAIR:
-// `release_bar` is the shared::cluster address of the accumulator-empty
-// barrier of the pair's even CTA, and a CTA whose 128 rows all lie past m
-// (its half of a pair tile over a short group) only releases.
-template <int BN, int CAP, bool DEV, bool PAIR = false>
+// null `buf` stores each row's 64 bytes straight from registers. CTA pairs
+// (CLU 1): `release_bar` is the shared::cluster address of the
+// accumulator-empty barrier of the pair's even CTA. In clusters, a CTA whose
+// 128 rows all lie past m (its half of a 256-row tile over a short group)
+// only releases.
+template <int BN, int CAP, bool DEV, int CLU = 0>
 __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, const Segment &sg, const GInfo &gi,
                                               const int kind, const int quarter, const int lane,
                                               const uint32_t t_acc, const int c0, const int c1, uint8_t *buf,
                                               const uint8_t *smem, const int part_stage0, const int pieces,
                                               const uint32_t release_bar = 0) {
-    using C = Cfg<BN, CAP, PAIR>;
+    using C = Cfg<BN, CAP, CLU>;
     auto release = [&]() {
-        if constexpr (PAIR)
+        if constexpr (CLU == 1)
             ptx::mbar_arrive_cluster(release_bar);
         else
             ptx::mbar_arrive(release_bar);
@@ -620,21 +634,24 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, con
     }
 }
 
-template <int BN, int CAP, bool DEV, bool PAIR>
+template <int BN, int CAP, bool DEV, int CLU>
 __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams<CAP, DEV> p) {
-    using C = Cfg<BN, CAP, PAIR>;
+    using C = Cfg<BN, CAP, CLU>;
+    constexpr bool CLUSTER = C::kCluster;  // clusters of two CTAs (either mode)
+    constexpr bool PAIR = C::kPairMma;     // CTA pair with cta_group::2 MMAs
+    constexpr bool MCAST = C::kMcast;      // multicast cluster
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t smem_base = ptx::smem_addr(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int group_count = p.group_count;
-    // CTA pairs (clusters of two): this CTA's rank in its pair; the schedule
-    // deals tiles to pairs (slot = pair index), and both CTAs of a pair walk
-    // the same tiles, each its own 128 rows
-    const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
-    const int slot = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-    const int nslots = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    // Clusters of two: this CTA's rank in its cluster; the schedule deals
+    // tiles to clusters (slot = cluster index), and both CTAs of a cluster walk
+    // the same 256-row tiles, each its own 128 rows
+    const uint32_t rank = CLUSTER ? ptx::cluster_ctarank() : 0u;
+    const int slot = CLUSTER ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int nslots = CLUSTER ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     // descriptors are patched in this call (host table: only those that changed)
     const bool publish = DEV || p.desc_maps != 0;
     // Tag of this call's partial-tile flags: one more than the last completed
@@ -668,11 +685,13 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     volatile int *s_epi_ok = reinterpret_cast<volatile int *>(bar_area + 208);  // [3]: by segment parity, tail
     volatile uint32_t *s_epoch = reinterpret_cast<volatile uint32_t *>(bar_area + 224);  // this call's epoch
     TailState *s_tail = reinterpret_cast<TailState *>(bar_area + 256);
-    // the other CTA's abort flag (CTA pairs), set with this CTA's
-    const uint32_t peer_abort = PAIR ? ptx::mapa(ptx::smem_addr(bar_area + 196), rank ^ 1u) : 0u;
-    // the odd CTA of a pair: its stage-empty and accumulator-full barriers are
-    // completed by the even CTA's tcgen05 commits
-    const bool remote_commits = PAIR && rank != 0;
+    // the other CTA's abort flag (clusters), set with this CTA's
+    const uint32_t peer_abort = CLUSTER ? ptx::mapa(ptx::smem_addr(bar_area + 196), rank ^ 1u) : 0u;
+    // barriers completed by the other CTA's tcgen05 commits: the odd CTA of a
+    // pair (stage-empty, accumulator-full); both CTAs of a multicast cluster
+    // (stage-empty: a stage is refilled once both CTAs' MMAs are done with it)
+    const bool remote_empty = (PAIR && rank != 0) || MCAST;
+    const bool remote_accf = PAIR && rank != 0;
     static_assert(256 + sizeof(TailState) <= 384, "barrier area");
     uint8_t *epi_stage = bar_area + C::kBarrierBytes;                // [4 warps][32 rows][64 B]
     int32_t *prefix;
@@ -683,10 +702,10 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     int32_t *wprefix = prefix + (C::kSmemPrefix ? C::kPrefixInts : (int)(cta_prefix_bytes(CAP) / 8));
 
     // ---- set-up -------------------------------------------------------------
-    // CTA pairs: every thread arrives on the cluster barrier (warp 4 once the
+    // Clusters: every thread arrives on the cluster barrier (warp 4 once the
     // mbarriers are initialised) and waits on it before its first access to
     // the other CTA
-    if constexpr (PAIR) {
+    if constexpr (CLUSTER) {
         if (warp != 4 && warp != 5)
             ptx::cluster_arrive();
     }
@@ -694,7 +713,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
         if (lane == 0) {
             for (int s = 0; s < C::kStages; ++s) {
                 ptx::mbar_init(full_bar(s), 1);
-                ptx::mbar_init(empty_bar(s), 1);
+                ptx::mbar_init(empty_bar(s), MCAST ? 2 : 1);  // multicast: both CTAs' MMAs
                 ptx::mbar_init(sff_bar(s), 4);
                 ptx::mbar_init(sfl_bar(s), 1);
             }
@@ -716,7 +735,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             s_tail->pieces = 0;
             ptx::fence_mbar_init();
         }
-        if constexpr (PAIR) {
+        if constexpr (CLUSTER) {
             __syncwarp();
             ptx::cluster_arrive();
         }
@@ -774,11 +793,11 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
         __syncwarp();
         ptx::named_barrier(2, 96);
         ptx::named_barrier_arrive(3, C::kThreads);
-        if constexpr (PAIR)
+        if constexpr (CLUSTER)
             ptx::cluster_wait();
     } else if (warp == 5) {
         // a pair's allocation is made by this warp of both CTAs together
-        if constexpr (PAIR) {
+        if constexpr (CLUSTER) {
             ptx::cluster_arrive();
             ptx::cluster_wait();
         }
@@ -865,7 +884,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     }
     uint32_t tmem_base = 0;  // warp 4 reads it after the role loops
     if (warp != 4) {
-        if constexpr (PAIR) {
+        if constexpr (CLUSTER) {
             if (warp != 5)
                 ptx::cluster_wait();
         }
@@ -885,8 +904,8 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     int split_tile = p.split_tile;
     if constexpr (DEV)
         split_tile = choose_split_tile(total_tiles, nslots, p.ws.partial_slots >= nslots ? p.split : 0);
-    if constexpr (PAIR)
-        split_tile = total_tiles;  // pairs run whole tiles only
+    if constexpr (CLUSTER)
+        split_tile = total_tiles;  // clusters run whole tiles only
     const int split = split_tile < total_tiles ? 1 : 0;
     const int P = (split && split_tile == 0 && total_work < nslots) ? total_work : nslots;
     const int sk0 = split_tile == 0 ? 0
@@ -898,7 +917,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     const int Psk = split ? (total_work - sk0 < P ? total_work - sk0 : P) : 0;
     // first schedule unit of CTA c's part of the split range
     auto sk_begin = [&](int c) { return sk0 + split_begin(c, Psk, total_work - sk0); };
-    Cursor<BN, CAP, DEV, PAIR> cursor0{prefix, wprefix, group_count, slot, split_tile, P, 0, 0, 0, (int)rank};
+    Cursor<BN, CAP, DEV, CLUSTER> cursor0{prefix, wprefix, group_count, slot, split_tile, P, 0, 0, 0, (int)rank};
     if (split && slot < Psk) {
         cursor0.w = sk_begin(slot);
         cursor0.w_end = sk_begin(slot + 1);
@@ -937,7 +956,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             bool any = false;
             while (ok && cur.next(p, sg)) {
                 any = true;
-                const GInfo gi = group_info<BN, PAIR>(load_group(p, sg.g));
+                const GInfo gi = group_info<BN, CLUSTER>(load_group(p, sg.g));
                 const int k_tiles = gi.k_tiles;
                 const int kend = sg.kt1 < k_tiles ? sg.kt1 : k_tiles;
                 if (sg.kt0 >= kend)
@@ -957,7 +976,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                 }
                 // a CTA of a pair whose 128 rows all lie past m loads no A and
                 // no A scales (its accumulator rows are never stored)
-                const bool a_live = !PAIR || sg.tm * kBlockM < gi.m;
+                const bool a_live = !CLUSTER || sg.tm * kBlockM < gi.m;
                 const uint8_t *sfa = gi.sfa + (size_t)sg.b * gi.sfa_batch + (size_t)sg.tm * k_blocks * kSfAtomBytes;
                 int sfb_blocks = gi.sf_row_blocks_b - sg.tn * C::kSfbRowBlocks;
                 sfb_blocks = sfb_blocks < C::kSfbRowBlocks ? sfb_blocks : C::kSfbRowBlocks;
@@ -966,7 +985,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                 for (int kt = sg.kt0; kt < kend; ++kt) {
                     // (the odd CTA of a pair is released by the even CTA's commits)
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns, p.ws.status,
-                                      kStatusProducerTimeout, peer_abort, remote_commits)) {
+                                      kStatusProducerTimeout, peer_abort, remote_empty)) {
                         ok = false;
                         break;
                     }
@@ -988,9 +1007,17 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                         if (a_live)
                             ptx::bulk_load(st + C::kABytes + C::kBBytes, sfa + (size_t)(4 * kt) * kSfAtomBytes,
                                            sf_bytes, sb, pol_a);
-                        ptx::tma_load_2d(st + C::kABytes + C::kBBytes + C::kSfaBytes, tmap_sfb,
-                                         kt * (4 * kSfAtomBytes / 8), sg.b * gi.sf_row_blocks_b + sg.tn * 2, sb,
-                                         pol_b);
+                        // (multicast cluster: the odd CTA fetches the B scales for both)
+                        if constexpr (MCAST) {
+                            if (rank == 1)
+                                ptx::tma_load_2d_multicast(st + C::kABytes + C::kBBytes + C::kSfaBytes, tmap_sfb,
+                                                           kt * (4 * kSfAtomBytes / 8),
+                                                           sg.b * gi.sf_row_blocks_b + sg.tn * 2, sb, 3, pol_b);
+                        } else {
+                            ptx::tma_load_2d(st + C::kABytes + C::kBBytes + C::kSfaBytes, tmap_sfb,
+                                             kt * (4 * kSfAtomBytes / 8), sg.b * gi.sf_row_blocks_b + sg.tn * 2, sb,
+                                             pol_b);
+                        }
                     } else {
                         ptx::mbar_arrive_expect_tx(sb, sf_bytes * (1 + sfb_blocks));
                         ptx::bulk_load(st + C::kABytes + C::kBBytes, sfa + (size_t)(4 * kt) * kSfAtomBytes, sf_bytes,
@@ -1006,8 +1033,15 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                     // a pair loads its half of the tile's B rows.
                     if (a_live)
                         ptx::tma_load_2d(st, tmap_a, kt * 128, sg.b * gi.m + sg.tm * kBlockM, fb, pol_a);
-                    ptx::tma_load_2d(st + C::kABytes, tmap_b, kt * 128,
-                                     sg.b * gi.n + sg.tn * BN + (int)rank * C::kBRows, fb, pol_b);
+                    if constexpr (MCAST) {
+                        // the even CTA fetches the B tile for both
+                        if (rank == 0)
+                            ptx::tma_load_2d_multicast(st + C::kABytes, tmap_b, kt * 128, sg.b * gi.n + sg.tn * BN, fb,
+                                                       3, pol_b);
+                    } else {
+                        ptx::tma_load_2d(st + C::kABytes, tmap_b, kt * 128,
+                                         sg.b * gi.n + sg.tn * BN + (PAIR ? (int)rank * C::kBRows : 0), fb, pol_b);
+                    }
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::kStages) {
@@ -1049,7 +1083,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                 s_tail->pieces = pieces;
                 if (flags_ok) {
                     ptx::fence_proxy_async_global();
-                    const int nch = tile_chunks<BN>(group_info<BN, PAIR>(load_group(p, sg.g)), sg);
+                    const int nch = tile_chunks<BN>(group_info<BN, CLUSTER>(load_group(p, sg.g)), sg);
                     const char *src =
                         reinterpret_cast<const char *>(p.ws.partials) + (size_t)(cta + 1) * kPartialSlotBytes;
                     bool good = true;
@@ -1100,7 +1134,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                 auto cur = cursor0;
                 Segment sg;
                 while (ok && cur.next(p, sg)) {
-                    const GInfo gi = group_info<BN, PAIR>(load_group(p, sg.g));
+                    const GInfo gi = group_info<BN, CLUSTER>(load_group(p, sg.g));
                     const int kend = sg.kt1 < gi.k_tiles ? sg.kt1 : gi.k_tiles;
                     for (int kt = sg.kt0; kt < kend; ++kt) {
                         if (!wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status,
@@ -1128,7 +1162,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             auto cur = cursor0;
             Segment sg;
             while (ok && cur.next(p, sg)) {
-                const GInfo gi = group_info<BN, PAIR>(load_group(p, sg.g));
+                const GInfo gi = group_info<BN, CLUSTER>(load_group(p, sg.g));
                 const int k_tiles = gi.k_tiles;
                 const int k_blocks = gi.k_blocks;
                 const int kend = sg.kt1 < k_tiles ? sg.kt1 : k_tiles;
@@ -1137,6 +1171,9 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                     break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::kAccCols);
+                // (multicast cluster: a CTA whose rows all lie past m computes
+                // nothing, but still releases its stages)
+                const bool mma_live = !MCAST || sg.tm * kBlockM < gi.m;
                 for (int kt = sg.kt0; kt < kend; ++kt) {
                     if (!wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status,
                                             kStatusMmaTimeout, peer_abort) ||
@@ -1154,15 +1191,21 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                     const uint32_t sfb_t = sfa_t + C::kSfaCols;
                     const uint64_t adesc = ptx::sdesc_kmajor_sw128(st);
                     const uint64_t bdesc = ptx::sdesc_kmajor_sw128(st + C::kABytes);
-                    for (int kb = 0; kb < nkb; ++kb) {
+                    for (int kb = 0; kb < (mma_live ? nkb : 0); ++kb) {
                         // +32 bytes per 64-element k-block inside the swizzled row
                         ptx::tc_mma_mxf4nvf4<C::kCtaGroup>(d_tmem, adesc + 2u * kb, bdesc + 2u * kb, C::kIdesc,
                                                            sfa_t + 4 * kb, sfb_t + kb * (BN / 32),
                                                            (kt != sg.kt0 || kb != 0) ? 1u : 0u);
                     }
-                    ptx::tc_commit<C::kCtaGroup>(empty_bar(stage));
-                    if constexpr (PAIR)
-                        ptx::tc_commit<C::kCtaGroup>(ptx::mapa(empty_bar(stage), 1u));
+                    if constexpr (MCAST) {
+                        // the stage is refilled (by multicasts into both CTAs)
+                        // once both CTAs' MMAs are done with it
+                        ptx::tc_commit_multicast(empty_bar(stage), 3);
+                    } else {
+                        ptx::tc_commit<C::kCtaGroup>(empty_bar(stage));
+                        if constexpr (PAIR)
+                            ptx::tc_commit<C::kCtaGroup>(ptx::mapa(empty_bar(stage), 1u));
+                    }
                     if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -1197,7 +1240,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
         auto cur = cursor0;
         Segment sg;
         while (ok && cur.next(p, sg)) {
-            const GInfo gi = group_info<BN, PAIR>(load_group(p, sg.g));
+            const GInfo gi = group_info<BN, CLUSTER>(load_group(p, sg.g));
             const int k_tiles = gi.k_tiles;
             const int k_blocks = gi.k_blocks;
             const int kend = sg.kt1 < k_tiles ? sg.kt1 : k_tiles;
@@ -1279,14 +1322,14 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             Segment nx;
             if (!cur.next(p, nx))
                 break;
-            const GInfo gi = group_info<BN, PAIR>(load_group(p, sg.g));
+            const GInfo gi = group_info<BN, CLUSTER>(load_group(p, sg.g));
             // a first piece of a split tile is always a CTA's last segment
             const int kind = sg.kt0 > 0 ? kEpiCont : kEpiWhole;
             // One thread waits for the accumulator; the eight warps leave or
             // stay together (the TMEM loads are warp-collective).
             if (threadIdx.x == 0)
                 s_epi_ok[it & 1] = wait_bounded(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns, p.ws.status,
-                                                kStatusEpilogueTimeout, peer_abort, remote_commits)
+                                                kStatusEpilogueTimeout, peer_abort, remote_accf)
                                        ? 1
                                        : 0;
             ptx::named_barrier(4, 256);
@@ -1300,7 +1343,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             // a whole tile releases the accumulator once its chunks are in
             // registers; a partial tile (fp32) goes out chunk by chunk first
             const uint32_t t_acc = tmem_base + (uint32_t)(acc * C::kAccCols);
-            epilogue_warp<BN, CAP, DEV, PAIR>(p, sg, gi, kind, quarter, lane, t_acc, first_half ? 0 : half,
+            epilogue_warp<BN, CAP, DEV, CLU>(p, sg, gi, kind, quarter, lane, t_acc, first_half ? 0 : half,
                                    first_half ? half : nch, first_half ? epi_stage + warp * C::kEpiStageBytes : nullptr,
                                    smem, 0, 0, kind == kEpiWhole ? acce_release(acc) : 0u);
             if (kind != kEpiWhole) {
@@ -1347,11 +1390,11 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     if (warp < 8) {
         const TailState ts = *s_tail;
         const Segment sg = ts.seg;
-        const GInfo gi = group_info<BN, PAIR>(load_group(p, ts.valid ? sg.g : 0));
+        const GInfo gi = group_info<BN, CLUSTER>(load_group(p, ts.valid ? sg.g : 0));
         const int kind = sg.kt0 > 0 ? kEpiCont : ((split && sg.kt1 < sg.ktg) ? kEpiFinish : kEpiWhole);
         if (threadIdx.x == 0) {
             int ok = ts.valid && wait_bounded(accf_bar(ts.acc), (uint32_t)ts.acc_phase, abort_flag, p.timeout_ns,
-                                              p.ws.status, kStatusEpilogueTimeout, peer_abort, remote_commits);
+                                              p.ws.status, kStatusEpilogueTimeout, peer_abort, remote_accf);
             if (ts.part_state) {
                 // the partial-tile copies must land before the CTA exits, even
                 // after an abort
@@ -1379,7 +1422,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             const int quarter = warp & 3;
             uint8_t *buf = warp < 4 ? epi_stage + warp * C::kEpiStageBytes
                                     : smem + (warp - 4) * C::kStageBytes + C::kStageBytes - C::kEpiStageBytes;
-            epilogue_warp<BN, CAP, DEV, PAIR>(p, sg, gi, kind, quarter, lane, tmem_base + (uint32_t)(ts.acc * C::kAccCols),
+            epilogue_warp<BN, CAP, DEV, CLU>(p, sg, gi, kind, quarter, lane, tmem_base + (uint32_t)(ts.acc * C::kAccCols),
                                    warp < 4 ? 0 : half, warp < 4 ? half : nch, buf, smem, ts.part_stage0,
                                    ts.pieces);
             if (kind == kEpiCont) {
@@ -1393,11 +1436,12 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     }
 
     // ---- teardown ----------------------------------------------------------
-    // CTA pairs: neither CTA leaves (or frees the pair's TMEM, which both free
-    // together) while the other may still touch its shared memory or TMEM
+    // Clusters: neither CTA leaves (or frees a pair's TMEM, which both free
+    // together) while the other may still touch its shared memory, barriers
+    // or TMEM
     ptx::tc_fence_before();
     __syncthreads();
-    if constexpr (PAIR) {
+    if constexpr (CLUSTER) {
         ptx::cluster_arrive();
         ptx::cluster_wait();
     }
@@ -1407,7 +1451,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     }
 }
 
-template <int BN, int CAP, bool DEV, bool PAIR = false>
+template <int BN, int CAP, bool DEV, int CLU = 0>
 cudaError_t launch_cap(const GemmLaunch &cfg, const GroupArgs *groups, const WorkspaceView &ws,
                        const void *tmpl_a, const void *tmpl_b, const void *tmpl_sfb, cudaStream_t stream) {
     static_assert(sizeof(GemmParams<CAP, DEV>) <= 32000, "kernel parameter limit");
@@ -1435,8 +1479,8 @@ cudaError_t launch_cap(const GemmLaunch &cfg, const GroupArgs *groups, const Wor
     }
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)cfg.grid, 1, 1);
-    lc.blockDim = dim3(Cfg<BN, CAP, PAIR>::kThreads, 1, 1);
-    lc.dynamicSmemBytes = Cfg<BN, CAP, PAIR>::kSmemBytes;
+    lc.blockDim = dim3(Cfg<BN, CAP, CLU>::kThreads, 1, 1);
+    lc.dynamicSmemBytes = Cfg<BN, CAP, CLU>::kSmemBytes;
     lc.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
@@ -1446,31 +1490,34 @@ cudaError_t launch_cap(const GemmLaunch &cfg, const GroupArgs *groups, const Wor
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     lc.attrs = attr;
-    lc.numAttrs = PAIR ? 2 : 1;
-    return cudaLaunchKernelEx(&lc, grouped_gemm_kernel<BN, CAP, DEV, PAIR>, prm);
+    lc.numAttrs = CLU ? 2 : 1;
+    return cudaLaunchKernelEx(&lc, grouped_gemm_kernel<BN, CAP, DEV, CLU>, prm);
 }
 
 }  // namespace
 
 cudaError_t prepare_gemm_kernels(int /*device*/) {
     cudaError_t e = cudaSuccess;
-#define NVFP4_SET_SMEM(BN, CAP, DEV, PAIR)                                                          \
+#define NVFP4_SET_SMEM(BN, CAP, DEV, CLU)                                                           \
     if (e == cudaSuccess)                                                                           \
-        e = cudaFuncSetAttribute(grouped_gemm_kernel<BN, CAP, DEV, PAIR>,                           \
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN, CAP, PAIR>::kSmemBytes);
-    NVFP4_SET_SMEM(128, kSmallGroups, false, false)
-    NVFP4_SET_SMEM(128, kMediumGroups, false, false)
-    NVFP4_SET_SMEM(128, NVFP4_MAX_GROUPS, false, false)
-    NVFP4_SET_SMEM(256, kSmallGroups, false, false)
-    NVFP4_SET_SMEM(256, kMediumGroups, false, false)
-    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS, false, false)
-    NVFP4_SET_SMEM(128, kMediumGroups, true, false)
-    NVFP4_SET_SMEM(128, NVFP4_MAX_GROUPS, true, false)
-    NVFP4_SET_SMEM(256, kMediumGroups, true, false)
-    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS, true, false)
-    NVFP4_SET_SMEM(256, kSmallGroups, false, true)
-    NVFP4_SET_SMEM(256, kMediumGroups, false, true)
-    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS, false, true)
+        e = cudaFuncSetAttribute(grouped_gemm_kernel<BN, CAP, DEV, CLU>,                            \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN, CAP, CLU>::kSmemBytes);
+    NVFP4_SET_SMEM(128, kSmallGroups, false, 0)
+    NVFP4_SET_SMEM(128, kMediumGroups, false, 0)
+    NVFP4_SET_SMEM(128, NVFP4_MAX_GROUPS, false, 0)
+    NVFP4_SET_SMEM(256, kSmallGroups, false, 0)
+    NVFP4_SET_SMEM(256, kMediumGroups, false, 0)
+    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS, false, 0)
+    NVFP4_SET_SMEM(128, kMediumGroups, true, 0)
+    NVFP4_SET_SMEM(128, NVFP4_MAX_GROUPS, true, 0)
+    NVFP4_SET_SMEM(256, kMediumGroups, true, 0)
+    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS, true, 0)
+    NVFP4_SET_SMEM(256, kSmallGroups, false, 1)
+    NVFP4_SET_SMEM(256, kMediumGroups, false, 1)
+    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS, false, 1)
+    NVFP4_SET_SMEM(256, kSmallGroups, false, 2)
+    NVFP4_SET_SMEM(256, kMediumGroups, false, 2)
+    NVFP4_SET_SMEM(256, NVFP4_MAX_GROUPS, false, 2)
 #undef NVFP4_SET_SMEM
     return e;
 }
@@ -1480,8 +1527,8 @@ int pair_capacity(int /*device*/) {
     // sums in shared memory) bounds how many pairs are resident at once.
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(2, 1, 1);
-    lc.blockDim = dim3(Cfg<256, kMediumGroups, true>::kThreads, 1, 1);
-    lc.dynamicSmemBytes = Cfg<256, kMediumGroups, true>::kSmemBytes;
+    lc.blockDim = dim3(Cfg<256, kMediumGroups, 2>::kThreads, 1, 1);
+    lc.dynamicSmemBytes = Cfg<256, kMediumGroups, 2>::kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -1490,7 +1537,7 @@ int pair_capacity(int /*device*/) {
     lc.attrs = attr;
     lc.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, (void *)grouped_gemm_kernel<256, kMediumGroups, false, true>, &lc) !=
+    if (cudaOccupancyMaxActiveClusters(&clusters, (void *)grouped_gemm_kernel<256, kMediumGroups, false, 2>, &lc) !=
         cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
@@ -1507,14 +1554,20 @@ cudaError_t launch_grouped(const GemmLaunch &cfg, const GroupArgs *groups, const
     if (cfg.group_count > kMediumGroups && ws.prefix_slots < cfg.grid)
         return cudaErrorInvalidValue;
     const bool wide = cfg.block_n == 256;
-    if (cfg.pair) {
-        if (!wide || cfg.device_table || cfg.split || (cfg.grid & 1))
+    if (cfg.cluster != 0) {
+        if (!wide || cfg.device_table || cfg.split || (cfg.grid & 1) || cfg.cluster > 2)
             return cudaErrorInvalidValue;
-        if (cfg.group_count <= kSmallGroups)
-            return launch_cap<256, kSmallGroups, false, true>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream);
-        if (cfg.group_count <= kMediumGroups)
-            return launch_cap<256, kMediumGroups, false, true>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream);
-        return launch_cap<256, NVFP4_MAX_GROUPS, false, true>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream);
+#define NVFP4_LAUNCH_CLUSTER(CLU)                                                                                   \
+    if (cfg.group_count <= kSmallGroups)                                                                          \
+        return launch_cap<256, kSmallGroups, false, CLU>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream);     \
+    if (cfg.group_count <= kMediumGroups)                                                                         \
+        return launch_cap<256, kMediumGroups, false, CLU>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream);    \
+    return launch_cap<256, NVFP4_MAX_GROUPS, false, CLU>(cfg, groups, ws, tmpl_a, tmpl_b, tmpl_sfb, stream);
+        if (cfg.cluster == 1) {
+            NVFP4_LAUNCH_CLUSTER(1)
+        }
+        NVFP4_LAUNCH_CLUSTER(2)
+#undef NVFP4_LAUNCH_CLUSTER
     }
     if (cfg.device_table) {
         // shared-memory prefix sums up to kMediumGroups groups

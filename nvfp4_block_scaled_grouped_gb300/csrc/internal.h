@@ -190,7 +190,8 @@ struct GemmLaunch {
     int capacity;           // workspace descriptor capacity (groups)
     uint64_t timeout_ns;    // bound of every wait
     bool device_table;      // the group table is `dt` (device memory), not the host array
-    bool pair;              // CTA pairs (clusters of two, 256 x 256 tiles, whole tiles only); grid = 2 x pairs
+    int cluster;            // clusters of two CTAs (256 x 256 tiles, whole tiles only; grid = 2 x clusters):
+                            // 0 none, 1 CTA pair with cta_group::2 MMAs, 2 multicast cluster
     DeviceTable dt;
 };
 
@@ -199,8 +200,8 @@ struct GemmLaunch {
 cudaError_t launch_grouped(const GemmLaunch &cfg, const GroupArgs *groups, const WorkspaceView &ws,
                            const void *tmpl_a, const void *tmpl_b, const void *tmpl_sfb, cudaStream_t stream);
 cudaError_t prepare_gemm_kernels(int device);
-// CTA pairs of the pair kernel that are resident at once on the current
-// device (0: the pair kernel cannot run).
+// Clusters of two CTAs of the cluster kernels that are resident at once on
+// the current device (0: the cluster kernels cannot run).
 int pair_capacity(int device);
 
 // Host layer (api.cu), shared by the entry points.

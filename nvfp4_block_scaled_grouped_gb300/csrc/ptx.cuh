@@ -150,6 +150,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         : "memory");
 }
 
+// 2-D tiled tensor load multicast to the CTAs of `cta_mask` in this cluster:
+// each receives the tile at shared-memory offset `dst` and its mbarrier at
+// offset `bar` (both given as this CTA's addresses) completes the bytes.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void *tmap, int32_t x, int32_t y,
+                                                      uint32_t bar, uint16_t cta_mask, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar), "h"(cta_mask), "l"(policy)
+        : "memory");
+}
+
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
                                           uint64_t policy) {
@@ -255,6 +267,15 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
     else
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                      : "memory");
+}
+
+// As tc_commit, arriving on the mbarrier at offset `bar` in every CTA of
+// `cta_mask` in this cluster.
+__device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // D(tmem) (+)= A(smem) * B(smem) with per-16-element e4m3 scales read from

@@ -1,7 +1,9 @@
-"""GPU parity of the CTA-pair kernel (clusters of two CTAs, 256 x 256 tiles,
-tcgen05 cta_group::2 MMAs) against the CPU oracle, through the C ABI.
+"""GPU parity of the cluster kernels (clusters of two CTAs, 256 x 256 tiles)
+against the CPU oracle, through the C ABI: the CTA pair (tcgen05 cta_group::2
+MMAs, NVFP4_PAIR=1) and the multicast cluster (each CTA its own 128 x 256
+tile, the B tile and its scales multicast to both, NVFP4_PAIR=2).
 
-NVFP4_PAIR=1 forces the pair kernel on every call that runs whole tiles;
+NVFP4_PAIR selects the cluster kernel on every call that runs whole tiles;
 the shapes put the second CTA of a pair on rows past m (groups with m <= 128),
 the second half of B past n (n mod 256 <= 128), M / N / K tails, batches
 (l > 1), empty groups and k == 0, and compare every output with the oracle.
@@ -27,12 +29,12 @@ def nv():
     return nv
 
 
-@pytest.fixture(autouse=True)
-def _pair(nv, monkeypatch):
-    monkeypatch.setenv("NVFP4_PAIR", "1")
+@pytest.fixture(autouse=True, params=["1", "2"], ids=["pair", "mcast"])
+def mode(request, nv, monkeypatch):
+    monkeypatch.setenv("NVFP4_PAIR", request.param)
     monkeypatch.delenv("NVFP4_SPLIT", raising=False)
     nv.set_tile_n(256)
-    yield
+    yield request.param
     nv.set_tile_n(0)
 
 
@@ -105,7 +107,7 @@ def test_pair_random_shapes(nv, oracle_mod):
         _run_full(nv, oracle_mod, _make(sizes, seed=9000 + call), f"pair random call {call}")
 
 
-def test_pair_many_waves_and_descriptor_reuse(nv, oracle_mod):
+def test_pair_many_waves_and_descriptor_reuse(nv, oracle_mod, mode):
     """More tiles than pairs (several tiles per pair), run twice (cached
     descriptors), then once through the one-CTA kernel on the same buffers
     (the B descriptor box changes) and once more as a pair."""
@@ -123,7 +125,7 @@ def test_pair_many_waves_and_descriptor_reuse(nv, oracle_mod):
         torch.cuda.synchronize()
         one = dp.c_host()
     finally:
-        os.environ["NVFP4_PAIR"] = "1"
+        os.environ["NVFP4_PAIR"] = mode
     ref = oracle_mod.grouped_gemm(prob.problem_sizes, prob.A, prob.B, prob.SFA, prob.SFB)
     for g, (c, r) in enumerate(zip(one, ref)):
         assert_parity(c, r, f"one-CTA kernel on the same buffers, group {g}")
