@@ -317,8 +317,11 @@ struct Segment {
     int w_tile_end;  // schedule index one past the tile's last unit
 };
 
-// First schedule unit of CTA c out of p in a split (stream-K) schedule.
+// First schedule unit of CTA c out of p in a split (stream-K) schedule
+// (0 <= c <= p); 32-bit arithmetic whenever c * total_work fits.
 __device__ __forceinline__ int split_begin(int c, int p, int total_work) {
+    if ((unsigned)total_work <= 0xffffffffu / (unsigned)p)
+        return (int)(((unsigned)c * (unsigned)total_work) / (unsigned)p);
     return (int)(((long long)c * total_work) / p);
 }
 
@@ -363,12 +366,16 @@ struct Cursor {
             phase = 1;
             if (w < w_end) {
                 // the range's first segment is the head when it is a later
-                // piece of a tile; otherwise it waits for phase 2
-                const int w0 = w;
-                split_segment(p, s, w_end);
-                if (s.kt0 > 0)
+                // piece of a tile (its first unit is not a tile's first
+                // k-tile); otherwise it waits for phase 2. Only the group and
+                // its k-tile count are needed to tell, not the whole segment,
+                // which lies on the path to the first copy.
+                const int g = find_group(wprefix, group_count, w);
+                const int kt = ceil_div_i(load_group(p, g).k, kBlockK);
+                if ((w - wprefix[g]) % (kt > 1 ? kt : 1) != 0) {
+                    split_segment(p, s, w_end);
                     return true;
-                w = w0;
+                }
             }
         }
         if (phase == 1) {
