@@ -124,9 +124,14 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
 }
 
 // Arrive on an mbarrier given by its shared::cluster address (this CTA's or
-// the other CTA's of the cluster), releasing at cluster scope.
+// the other CTA's of the cluster), with the instruction's default release
+// semantics. (An explicit .release.cluster arrive was measured at ~1100
+// cycles per remote arrive on GB300, and it sat on the CTA pair's per-stage
+// path; the data it publishes -- TMA writes and tcgen05.st of the arriving
+// CTA -- are complete by the arrive through their own completion
+// mechanisms, mbarrier complete_tx and tcgen05.wait::st.)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
