@@ -515,6 +515,48 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, con
                 dst[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
         }
     };
+    // A whole tile's row segments, held in registers (the warp's chunk c0 + i
+    // in hs[i], lane = row), go out as whole 128-byte lines: for each pair of
+    // chunks and each group q of 8 rows, lane 4x + p gathers by shuffles the
+    // 32-byte part p of row 8q + x (four rounds, one per part, in which the
+    // eight lanes of the row group send that part), so each store instruction
+    // writes 8 rows x 128 B -- a quarter of the write requests of one
+    // 16-byte piece per row, which is what the next tile's operand copies
+    // compete with.
+    auto store_lines = [&](const uint32_t (&hs)[C::kMaxLoopChunks][16]) {
+        const int x = lane >> 2, part = lane & 3;
+        const bool wide = (reinterpret_cast<uintptr_t>(c_base) & 31u) == 0;
+#pragma unroll
+        for (int cp = 0; cp < C::kMaxLoopChunks / 2; ++cp) {
+            if (c0 + 2 * cp >= c1)
+                break;
+            const int cc = c0 + 2 * cp + (part >> 1);
+            const int col = sg.tn * BN + cc * 32 + 16 * (part & 1);
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                uint32_t o[8];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t got = __shfl_sync(0xffffffffu, hs[2 * cp + (r >> 1)][8 * (r & 1) + j], 8 * q + x);
+                        if (r == 0 || part == r)
+                            o[j] = got;
+                    }
+                }
+                const int grow = sg.tm * kBlockM + quarter * 32 + 8 * q + x;
+                if (grow < m && cc < c1) {
+                    __half *dst = c_base + (size_t)grow * (size_t)n + col;
+                    if (wide) {
+                        ptx::st_global_v8(dst, o);
+                    } else {
+                        reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                        reinterpret_cast<uint4 *>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+            }
+        }
+    };
     auto pack = [](float x0, float x1) {
         __half2 h2 = __floats2half2_rn(x0, x1);
         return *reinterpret_cast<uint32_t *>(&h2);
@@ -611,15 +653,7 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, con
         __syncwarp();
         if (lane == 0)
             release();
-#pragma unroll
-        for (int i = 0; i < C::kMaxLoopChunks; ++i) {
-            if (c0 + i < c1) {
-                if (buf)
-                    store_chunk(c0 + i, hs[i]);
-                else
-                    store_direct(c0 + i, hs[i]);
-            }
-        }
+        store_lines(hs);
     } else {
         const bool zero = gi.k == 0;
         uint32_t h[16];

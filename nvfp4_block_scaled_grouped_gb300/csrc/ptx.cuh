@@ -194,6 +194,13 @@ __device__ __forceinline__ void tmap_acquire(const void *tmap) {
     asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(tmap) : "memory");
 }
 
+// 32-byte global store (sm_100 and later); dst must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *dst, const uint32_t (&v)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 // Start fetching a tensor map into the descriptor cache.
 __device__ __forceinline__ void tmap_prefetch(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
