@@ -42,10 +42,11 @@
 //                 chunks): tcgen05.ld of the accumulator lanes they own,
 //                 fp32 -> fp16 round-to-nearest-even; a whole tile is moved
 //                 into registers first and the accumulator released to the
-//                 next tile's MMAs before the stores (warps 0-3 stage theirs
-//                 through a swizzled per-warp buffer so each store writes 8
-//                 rows x 64 B, warps 10-13 store each row's 64 B from
-//                 registers); rows >= m and column chunks >= n skipped;
+//                 next tile's MMAs before the stores, which a warp-shuffle
+//                 transpose turns into 8 rows x 128 B per store instruction
+//                 (whole lines: few write requests, which would otherwise
+//                 hold up the next tile's copies); rows >= m and column
+//                 chunks >= n skipped;
 //       warps 0-7 epilogue of the CTA's last segment, once every role has
 //                 left its loop (the last epilogue is on the critical path).
 //
@@ -127,18 +128,16 @@ struct Cfg {
     // from 384
     static constexpr int kBarrierBytes = 448;
     static_assert(((kPairMma ? 4 : 3) * kStages + 2 * kAccStages) * 8 <= 176 && kStages <= 8, "barrier area");
-    static constexpr int kEpiStageBytes = 32 * 64;                 // per epilogue warp: 32 rows x 32 fp16
     // A finishing CTA receives the next piece's partial tile in ring stages,
     // kPartialChunksPerStage 16 KiB chunks (32 columns x 128 rows fp32) per
-    // stage from offset 0; the last kEpiStageBytes of stages 0..3 are the
-    // staging buffers of the four helper warps that join the last epilogue.
-    static constexpr int kPartialChunksPerStage = (kStageBytes - kEpiStageBytes) / kPartialChunkBytes;
+    // stage from offset 0.
+    static constexpr int kPartialChunksPerStage = kStageBytes / kPartialChunkBytes;
     static_assert(kStages >= 4 && kPartialChunksPerStage * kStages >= BN / 32, "partial tile in the ring");
     // Prefix sums live in shared memory for up to kMediumGroups groups, else
     // in the CTA's global scratch slot.
     static constexpr bool kSmemPrefix = CAP <= kMediumGroups;
     static constexpr int kPrefixInts = (int)round_up(CAP + 1, 4);
-    static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kBarrierBytes + 4 * kEpiStageBytes +
+    static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kBarrierBytes +
                                          (kSmemPrefix ? 2 * sizeof(int32_t) * kPrefixInts : 0);
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static constexpr uint32_t kIdesc = ptx::idesc_mxf4nvf4(kPairMma ? 2 * kBlockM : kBlockM, BN);
@@ -442,14 +441,12 @@ __device__ __forceinline__ int tile_chunks(const GInfo &gi, const Segment &sg) {
 }
 
 // One warp's share of a segment's epilogue: accumulator lanes 32 * quarter ..
-// +31 (tile rows), column chunks [c0, c1). TMEM loads run half a chunk (16
-// columns) ahead of the arithmetic and stores. `buf` is the warp's 2 KiB
-// staging buffer; `smem` the CTA's ring (holding the next piece's partial tile
-// from stage part_stage0 when finishing a split tile). With `release_bar` (a
-// whole tile in the main loop, at most kMaxLoopChunks chunks per warp) the
-// warp first moves its chunks from TMEM into registers and arrives on
-// release_bar, so the next tile's MMAs may start, and then stores them; a
-// null `buf` stores each row's 64 bytes straight from registers. CTA pairs
+// +31 (tile rows), column chunks [c0, c1) (at most kMaxLoopChunks). TMEM loads
+// run half a chunk (16 columns) ahead of the arithmetic. `smem` is the CTA's
+// ring (holding the next piece's partial tile from stage part_stage0 when
+// finishing a split tile). A whole tile is moved from TMEM into registers
+// first; with `release_bar` (the main loop) the warp then arrives on it, so
+// the next tile's MMAs may start, before the stores. CTA pairs
 // (CLU 1): `release_bar` is the shared::cluster address of the
 // accumulator-empty barrier of the pair's even CTA. In clusters, a CTA whose
 // 128 rows all lie past m (its half of a 256-row tile over a short group)
@@ -457,7 +454,7 @@ __device__ __forceinline__ int tile_chunks(const GInfo &gi, const Segment &sg) {
 template <int BN, int CAP, bool DEV, int CLU = 0>
 __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, const Segment &sg, const GInfo &gi,
                                               const int kind, const int quarter, const int lane,
-                                              const uint32_t t_acc, const int c0, const int c1, uint8_t *buf,
+                                              const uint32_t t_acc, const int c0, const int c1,
                                               const uint8_t *smem, const int part_stage0, const int pieces,
                                               const uint32_t release_bar = 0) {
     using C = Cfg<BN, CAP, CLU>;
@@ -483,76 +480,40 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, con
     const int row = sg.tm * kBlockM + r_local;
     const uint32_t t_row = t_acc + ((uint32_t)(quarter * 32) << 16);
     __half *c_base = static_cast<__half *>(gi.c) + (size_t)sg.b * (size_t)m * (size_t)n;
-    // fp16 row segment (64 B, 16 words) of chunk cc -> the staging buffer,
-    // 16-byte pieces XOR-swizzled by (row / 2) % 4 so that neither the
-    // row-wise writes nor the transposed reads conflict on banks; then 4 lanes
-    // per row, each store writing 8 rows x 64 B.
-    auto store_chunk = [&](const int cc, const uint32_t (&h)[16]) {
-        const int col = sg.tn * BN + cc * 32;
-        const int sw = (lane >> 1) & 3;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4 *>(buf + lane * 64 + 16 * (j ^ sw)) =
-                make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-        __syncwarp();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int r = 8 * q + (lane >> 2);
-            const int piece = lane & 3;
-            const uint4 val = *reinterpret_cast<const uint4 *>(buf + r * 64 + 16 * (piece ^ ((r >> 1) & 3)));
-            const int grow = sg.tm * kBlockM + quarter * 32 + r;
-            if (grow < m)
-                *reinterpret_cast<uint4 *>(c_base + (size_t)grow * (size_t)n + col + 8 * piece) = val;
-        }
-        __syncwarp();
-    };
-    // without a staging buffer: each lane writes its row's 64 bytes
-    auto store_direct = [&](const int cc, const uint32_t (&h)[16]) {
-        if (row < m) {
-            uint4 *dst = reinterpret_cast<uint4 *>(c_base + (size_t)row * (size_t)n + sg.tn * BN + cc * 32);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                dst[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-        }
-    };
-    // A whole tile's row segments, held in registers (the warp's chunk c0 + i
-    // in hs[i], lane = row), go out as whole 128-byte lines: for each pair of
-    // chunks and each group q of 8 rows, lane 4x + p gathers by shuffles the
+    // Two chunks of fp16 row segments held in registers (chunks c0 + 2cp and
+    // c0 + 2cp + 1 in h2[0], h2[1]; lane = row) go out as whole 128-byte
+    // lines: for each group q of 8 rows, lane 4x + p gathers by shuffles the
     // 32-byte part p of row 8q + x (four rounds, one per part, in which the
     // eight lanes of the row group send that part), so each store instruction
-    // writes 8 rows x 128 B -- a quarter of the write requests of one
-    // 16-byte piece per row, which is what the next tile's operand copies
-    // compete with.
-    auto store_lines = [&](const uint32_t (&hs)[C::kMaxLoopChunks][16]) {
+    // writes 8 rows x 128 B -- a quarter of the write requests of one 16-byte
+    // piece per row, which is what the next tile's operand copies compete
+    // with. (The q loop stays rolled: unrolled, it costs tens of KB of code
+    // per kernel, which every call fetches cold.)
+    auto store_pair = [&](const int cp, const uint32_t (&h2)[2][16]) {
         const int x = lane >> 2, part = lane & 3;
         const bool wide = (reinterpret_cast<uintptr_t>(c_base) & 31u) == 0;
-#pragma unroll
-        for (int cp = 0; cp < C::kMaxLoopChunks / 2; ++cp) {
-            if (c0 + 2 * cp >= c1)
-                break;
-            const int cc = c0 + 2 * cp + (part >> 1);
-            const int col = sg.tn * BN + cc * 32 + 16 * (part & 1);
+        const int cc = c0 + 2 * cp + (part >> 1);
+        const int col = sg.tn * BN + cc * 32 + 16 * (part & 1);
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                uint32_t o[8];
+        for (int q = 0; q < 4; ++q) {
+            uint32_t o[8];
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
+            for (int r = 0; r < 4; ++r) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t got = __shfl_sync(0xffffffffu, hs[2 * cp + (r >> 1)][8 * (r & 1) + j], 8 * q + x);
-                        if (r == 0 || part == r)
-                            o[j] = got;
-                    }
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t got = __shfl_sync(0xffffffffu, h2[r >> 1][8 * (r & 1) + j], 8 * q + x);
+                    if (r == 0 || part == r)
+                        o[j] = got;
                 }
-                const int grow = sg.tm * kBlockM + quarter * 32 + 8 * q + x;
-                if (grow < m && cc < c1) {
-                    __half *dst = c_base + (size_t)grow * (size_t)n + col;
-                    if (wide) {
-                        ptx::st_global_v8(dst, o);
-                    } else {
-                        reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                        reinterpret_cast<uint4 *>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
-                    }
+            }
+            const int grow = sg.tm * kBlockM + quarter * 32 + 8 * q + x;
+            if (grow < m && cc < c1) {
+                __half *dst = c_base + (size_t)grow * (size_t)n + col;
+                if (wide) {
+                    ptx::st_global_v8(dst, o);
+                } else {
+                    reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                    reinterpret_cast<uint4 *>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
                 }
             }
         }
@@ -586,8 +547,9 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, con
             put(vb, dst + ((size_t)cc * 8 + 4) * kBlockM);
         }
     } else if (kind == kEpiFinish) {
-        // the next piece's partial from the ring, any further ones (a tile
-        // spanning 3+ CTAs) from L2
+        // the first piece of a split tile (always the CTA's last segment):
+        // plus the next piece's partial from the ring, and any further ones
+        // (a tile spanning 3+ CTAs) from L2
         const float4 *gpart = reinterpret_cast<const float4 *>(p.ws.partials) + r_local;
         auto add_half = [&](const uint32_t (&v)[16], const int cc, const int q0, uint32_t *h) {
             const float4 *sp =
@@ -617,19 +579,30 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, con
                 h[2 * q + 1] = pack(__uint_as_float(v[4 * q + 2]) + a[q].z, __uint_as_float(v[4 * q + 3]) + a[q].w);
             }
         };
-        uint32_t h[16];
 #pragma unroll 1
-        for (int cc = c0; cc < c1; ++cc) {
-            ptx::tmem_ld_wait();
-            ptx::tmem_ld_32x32b_x16(t_row + cc * 32 + 16, vb);
-            add_half(va, cc, 0, h);
-            ptx::tmem_ld_wait();
-            if (cc + 1 < c1)
-                ptx::tmem_ld_32x32b_x16(t_row + (cc + 1) * 32, va);
-            add_half(vb, cc, 4, h + 8);
-            store_chunk(cc, h);
+        for (int cp = 0; c0 + 2 * cp < c1; ++cp) {
+            uint32_t h2[2][16];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int cc = c0 + 2 * cp + i;
+                if (cc < c1) {
+                    ptx::tmem_ld_wait();
+                    ptx::tmem_ld_32x32b_x16(t_row + cc * 32 + 16, vb);
+                    add_half(va, cc, 0, h2[i]);
+                    ptx::tmem_ld_wait();
+                    if (cc + 1 < c1)
+                        ptx::tmem_ld_32x32b_x16(t_row + (cc + 1) * 32, va);
+                    add_half(vb, cc, 4, h2[i] + 8);
+                }
+            }
+            store_pair(cp, h2);
         }
-    } else if (release_bar != 0) {
+    } else {
+        // whole tile: every chunk into registers; in the main loop the
+        // accumulator is then released to the next tile's MMAs before the
+        // stores. The pairs of chunks go out through one store_pair (the
+        // second pair moved down after the first is stored): a last segment
+        // runs this code once per call from a cold instruction cache.
         const bool zero = gi.k == 0;
         uint32_t hs[C::kMaxLoopChunks][16];
 #pragma unroll
@@ -649,28 +622,20 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, con
                     hs[i][8 + q] = zero ? 0u : pack(__uint_as_float(vb[2 * q]), __uint_as_float(vb[2 * q + 1]));
             }
         }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0)
-            release();
-        store_lines(hs);
-    } else {
-        const bool zero = gi.k == 0;
-        uint32_t h[16];
+        if (release_bar != 0) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                release();
+        }
 #pragma unroll 1
-        for (int cc = c0; cc < c1; ++cc) {
-            ptx::tmem_ld_wait();
-            ptx::tmem_ld_32x32b_x16(t_row + cc * 32 + 16, vb);
+        for (int cp = 0; cp < C::kMaxLoopChunks / 2 && c0 + 2 * cp < c1; ++cp) {
+            store_pair(cp, reinterpret_cast<const uint32_t(&)[2][16]>(hs[0]));
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                h[q] = zero ? 0u : pack(__uint_as_float(va[2 * q]), __uint_as_float(va[2 * q + 1]));
-            ptx::tmem_ld_wait();
-            if (cc + 1 < c1)
-                ptx::tmem_ld_32x32b_x16(t_row + (cc + 1) * 32, va);
+            for (int i = 0; i + 2 < C::kMaxLoopChunks; ++i)
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                h[8 + q] = zero ? 0u : pack(__uint_as_float(vb[2 * q]), __uint_as_float(vb[2 * q + 1]));
-            store_chunk(cc, h);
+                for (int w = 0; w < 16; ++w)
+                    hs[i][w] = hs[i + 2][w];
         }
     }
 }
@@ -734,10 +699,9 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     const bool remote_empty = (PAIR && rank != 0) || MCAST;
     const bool remote_accf = PAIR && rank != 0;
     static_assert(256 + sizeof(TailState) <= 384, "barrier area");
-    uint8_t *epi_stage = bar_area + C::kBarrierBytes;                // [4 warps][32 rows][64 B]
     int32_t *prefix;
     if constexpr (C::kSmemPrefix)
-        prefix = reinterpret_cast<int32_t *>(epi_stage + 4 * C::kEpiStageBytes);
+        prefix = reinterpret_cast<int32_t *>(bar_area + C::kBarrierBytes);
     else
         prefix = p.ws.cta_prefix + (size_t)blockIdx.x * (cta_prefix_bytes(CAP) / sizeof(int32_t));
     int32_t *wprefix = prefix + (C::kSmemPrefix ? C::kPrefixInts : (int)(cta_prefix_bytes(CAP) / 8));
@@ -1347,9 +1311,8 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
         // ================= epilogue (warps 0..3 and 10..13) =================
         // Every segment but the CTA's last; the last is finished below, once
         // every role has left its loop, by warps 0..7. Warp w takes TMEM lane
-        // quarter w % 4; warps 0..3 the first half of the column chunks
-        // (storing through their staging buffers), warps 10..13 the second
-        // (storing straight from registers).
+        // quarter w % 4; warps 0..3 the first half of the column chunks,
+        // warps 10..13 the second.
         const int cta = blockIdx.x;
         const bool first_half = warp < 4;
         const int quarter = warp & 3;
@@ -1385,8 +1348,8 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             // registers; a partial tile (fp32) goes out chunk by chunk first
             const uint32_t t_acc = tmem_base + (uint32_t)(acc * C::kAccCols);
             epilogue_warp<BN, CAP, DEV, CLU>(p, sg, gi, kind, quarter, lane, t_acc, first_half ? 0 : half,
-                                   first_half ? half : nch, first_half ? epi_stage + warp * C::kEpiStageBytes : nullptr,
-                                   smem, 0, 0, kind == kEpiWhole ? acce_release(acc) : 0u);
+                                             first_half ? half : nch, smem, 0, 0,
+                                             kind == kEpiWhole ? acce_release(acc) : 0u);
             if (kind != kEpiWhole) {
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -1422,8 +1385,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
 
     // ---- the last segment: warps 0..7 ------------------------------------------
     // Its MMAs are the CTA's last, so the ring holds nothing but the partial
-    // tile the producer may have prefetched; warps 4..7 stage their stores in
-    // the last 2 KiB of stages 0..3.
+    // tile the producer may have prefetched.
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -1461,11 +1423,9 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             const int nch = tile_chunks<BN>(gi, sg);
             const int half = (nch + 1) / 2;
             const int quarter = warp & 3;
-            uint8_t *buf = warp < 4 ? epi_stage + warp * C::kEpiStageBytes
-                                    : smem + (warp - 4) * C::kStageBytes + C::kStageBytes - C::kEpiStageBytes;
             epilogue_warp<BN, CAP, DEV, CLU>(p, sg, gi, kind, quarter, lane, tmem_base + (uint32_t)(ts.acc * C::kAccCols),
-                                   warp < 4 ? 0 : half, warp < 4 ? half : nch, buf, smem, ts.part_stage0,
-                                   ts.pieces);
+                                             warp < 4 ? 0 : half, warp < 4 ? half : nch, smem, ts.part_stage0,
+                                             ts.pieces);
             if (kind == kEpiCont) {
                 ptx::named_barrier(1, 256);
                 if (threadIdx.x == 0) {
