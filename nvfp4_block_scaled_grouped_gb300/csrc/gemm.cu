@@ -127,7 +127,7 @@ struct Cfg {
     // accumulator barriers from 0, scratch from 176, scales-landed per stage
     // from 384
     static constexpr int kBarrierBytes = 448;
-    static_assert(((kPairMma ? 4 : 3) * kStages + 2 * kAccStages) * 8 <= 176 && kStages <= 8, "barrier area");
+    static_assert((3 * kStages + 2 * kAccStages) * 8 <= 176 && kStages <= 8, "barrier area");
     // A finishing CTA receives the next piece's partial tile in ring stages,
     // kPartialChunksPerStage 16 KiB chunks (32 columns x 128 rows fp32) per
     // stage from offset 0.
@@ -677,7 +677,6 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     auto acce_bar = [&](int a) { return bars + 8u * (3 * C::kStages + C::kAccStages + a); };
     // CTA pairs, even CTA: the odd CTA's stage s is ready (A / B landed, its
     // scales written to its TMEM)
-    auto peer_bar = [&](int s) { return bars + 8u * (3 * C::kStages + 2 * C::kAccStages + s); };
     // where the epilogue releases accumulator a: the even CTA's barrier in a pair
     auto acce_release = [&](int a) { return PAIR ? ptx::mapa(acce_bar(a), 0u) : acce_bar(a); };
     const uint32_t drain_bar = bars + 176;    // the MMA thread's issued MMAs have completed
@@ -719,16 +718,13 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
             for (int s = 0; s < C::kStages; ++s) {
                 ptx::mbar_init(full_bar(s), 1);
                 ptx::mbar_init(empty_bar(s), MCAST ? 2 : 1);  // multicast: both CTAs' MMAs
-                ptx::mbar_init(sff_bar(s), 4);
+                // CTA pairs: the even CTA's also takes the odd CTA's relay
+                ptx::mbar_init(sff_bar(s), (PAIR && rank == 0) ? 5 : 4);
                 ptx::mbar_init(sfl_bar(s), 1);
             }
             for (int a = 0; a < C::kAccStages; ++a) {
                 ptx::mbar_init(accf_bar(a), 1);
                 ptx::mbar_init(acce_bar(a), PAIR ? 16 : 8);  // the epilogue warps of both CTAs of a pair
-            }
-            if constexpr (PAIR) {
-                for (int s = 0; s < C::kStages; ++s)
-                    ptx::mbar_init(peer_bar(s), 1);
             }
             ptx::mbar_init(partial_bar, 1);
             ptx::mbar_init(drain_bar, 1);
@@ -1130,8 +1126,9 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
     } else if (warp == 5) {
         if (PAIR && rank != 0) {
             // ============ relay (odd CTA of a pair) ============
-            // Tells the even CTA's MMA thread when this CTA's stage is ready:
-            // its A / B tiles have landed and its scale writers are done.
+            // Tells the even CTA's MMA thread when this CTA's stage is ready
+            // (its A / B tiles have landed and its scale writers are done) by
+            // arriving on the even CTA's scales-written barrier of the stage.
             if (lane == 0) {
                 int stage = 0;
                 uint32_t phase = 0;
@@ -1149,7 +1146,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                             ok = false;
                             break;
                         }
-                        ptx::mbar_arrive_cluster(ptx::mapa(peer_bar(stage), 0u));
+                        ptx::mbar_arrive_cluster(ptx::mapa(sff_bar(stage), 0u));
                         if (++stage == C::kStages) {
                             stage = 0;
                             phase ^= 1u;
@@ -1180,12 +1177,14 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                 // nothing, but still releases its stages)
                 const bool mma_live = !MCAST || sg.tm * kBlockM < gi.m;
                 for (int kt = sg.kt0; kt < kend; ++kt) {
-                    if (!wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status,
-                                            kStatusMmaTimeout, peer_abort) ||
-                        !wait_bounded(sff_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status,
-                                            kStatusMmaTimeout, peer_abort) ||
-                        (PAIR && !wait_bounded<true>(peer_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status,
-                                                     kStatusMmaTimeout, peer_abort, true))) {
+                    // (CTA pairs: one wait. The even CTA's scales-written
+                    // barrier completes once its tiles have landed too -- its
+                    // scale writer warp 6 waits for them -- and the odd CTA's
+                    // stage is ready, which the odd CTA's relay reports on it.)
+                    if ((!PAIR && !wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status,
+                                                kStatusMmaTimeout, peer_abort)) ||
+                        !wait_bounded<PAIR>(sff_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status,
+                                            kStatusMmaTimeout, peer_abort)) {
                         ok = false;
                         break;
                     }
@@ -1196,11 +1195,23 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                     const uint32_t sfb_t = sfa_t + C::kSfaCols;
                     const uint64_t adesc = ptx::sdesc_kmajor_sw128(st);
                     const uint64_t bdesc = ptx::sdesc_kmajor_sw128(st + C::kABytes);
-                    for (int kb = 0; kb < (mma_live ? nkb : 0); ++kb) {
-                        // +32 bytes per 64-element k-block inside the swizzled row
-                        ptx::tc_mma_mxf4nvf4<C::kCtaGroup>(d_tmem, adesc + 2u * kb, bdesc + 2u * kb, C::kIdesc,
-                                                           sfa_t + 4 * kb, sfb_t + kb * (BN / 32),
-                                                           (kt != sg.kt0 || kb != 0) ? 1u : 0u);
+                    // (+32 bytes per 64-element k-block inside the swizzled row)
+                    if (nkb == 4 && mma_live) {
+                        // a whole k-tile: straight-line issue (a loop with a
+                        // run-time trip count between the MMAs costs issue rate)
+                        ptx::tc_mma_mxf4nvf4<C::kCtaGroup>(d_tmem, adesc, bdesc, C::kIdesc, sfa_t, sfb_t,
+                                                           kt != sg.kt0 ? 1u : 0u);
+                        ptx::tc_mma_mxf4nvf4<C::kCtaGroup>(d_tmem, adesc + 2u, bdesc + 2u, C::kIdesc, sfa_t + 4,
+                                                           sfb_t + (BN / 32), 1u);
+                        ptx::tc_mma_mxf4nvf4<C::kCtaGroup>(d_tmem, adesc + 4u, bdesc + 4u, C::kIdesc, sfa_t + 8,
+                                                           sfb_t + 2 * (BN / 32), 1u);
+                        ptx::tc_mma_mxf4nvf4<C::kCtaGroup>(d_tmem, adesc + 6u, bdesc + 6u, C::kIdesc, sfa_t + 12,
+                                                           sfb_t + 3 * (BN / 32), 1u);
+                    } else {
+                        for (int kb = 0; kb < (mma_live ? nkb : 0); ++kb)
+                            ptx::tc_mma_mxf4nvf4<C::kCtaGroup>(d_tmem, adesc + 2u * kb, bdesc + 2u * kb, C::kIdesc,
+                                                               sfa_t + 4 * kb, sfb_t + kb * (BN / 32),
+                                                               (kt != sg.kt0 || kb != 0) ? 1u : 0u);
                     }
                     if constexpr (MCAST) {
                         // the stage is refilled (by multicasts into both CTAs)
@@ -1299,8 +1310,23 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
-                    ptx::mbar_arrive(sff_bar(stage));
+                // (the even CTA of a pair: warp 6 first waits for the stage's
+                // A and B tiles, so that the barrier stands for the whole
+                // stage and the pair's MMA thread waits on it alone)
+                int fine = 1;
+                if (lane == 0) {
+                    if (PAIR && rank == 0 && warp == 6)
+                        fine = wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, p.ws.status,
+                                            kStatusMmaTimeout, peer_abort)
+                                   ? 1
+                                   : 0;
+                    if (fine)
+                        ptx::mbar_arrive(sff_bar(stage));
+                }
+                if (PAIR && !__shfl_sync(0xffffffffu, fine, 0)) {
+                    ok = false;
+                    break;
+                }
                 if (++stage == C::kStages) {
                     stage = 0;
                     phase ^= 1u;
