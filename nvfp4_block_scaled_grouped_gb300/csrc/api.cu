@@ -330,6 +330,7 @@ int launch_on_workspace(int group_count, GroupArgs *args, long long total_tiles,
             total_tiles = pair_tiles;
             total_work = pair_work;
         }
+        cfg.pair_launch = cfg.cluster == 0 && cfg.grid % 2 == 0 && cfg.grid / 2 <= st->pairs;
         if (group_count > kMediumGroups && prefix_slots < cfg.grid)
             return fail(NVFP4_ERR_UNSUPPORTED, "workspace has %d CTA slots, the launch needs %d", prefix_slots,
                         cfg.grid);
@@ -420,6 +421,7 @@ int launch_device_table(int group_count, const DeviceTable &dt, int block_n, voi
     cfg.timeout_ns = watchdog_ns();
     cfg.device_table = true;
     cfg.cluster = 0;
+    cfg.pair_launch = cfg.grid % 2 == 0 && cfg.grid / 2 <= st->pairs;
     cfg.dt = dt;
     (void)state;  // region 0 and its host cache are left alone
     const WorkspaceView ws = second_region(workspace_view(ws_base, capacity, slots, slots, 2));

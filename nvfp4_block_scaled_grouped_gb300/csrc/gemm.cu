@@ -525,7 +525,8 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, con
     // Partial tiles: [chunk][quad q][row] of float4, so a warp's stores and
     // loads of one (chunk, q) cover 512 contiguous bytes.
     uint32_t va[16], vb[16];
-    ptx::tmem_ld_32x32b_x16(t_row + c0 * 32, va);
+    if (kind != kEpiWhole)
+        ptx::tmem_ld_32x32b_x16(t_row + c0 * 32, va);
     if (kind == kEpiCont) {
         float4 *dst = reinterpret_cast<float4 *>(p.ws.partials) + (size_t)cta * (kPartialSlotBytes / 16) + r_local;
         auto put = [&](const uint32_t (&v)[16], float4 *d) {
@@ -605,21 +606,18 @@ __device__ __forceinline__ void epilogue_warp(const GemmParams<CAP, DEV> &p, con
         // runs this code once per call from a cold instruction cache.
         const bool zero = gi.k == 0;
         uint32_t hs[C::kMaxLoopChunks][16];
+        // one 32-column load per chunk: the drain is a chain of TMEM load
+        // round trips, which gate the release of the accumulator
 #pragma unroll
         for (int i = 0; i < C::kMaxLoopChunks; ++i) {
             const int cc = c0 + i;
             if (cc < c1) {
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x32(t_row + cc * 32, v);
                 ptx::tmem_ld_wait();
-                ptx::tmem_ld_32x32b_x16(t_row + cc * 32 + 16, vb);
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    hs[i][q] = zero ? 0u : pack(__uint_as_float(va[2 * q]), __uint_as_float(va[2 * q + 1]));
-                ptx::tmem_ld_wait();
-                if (cc + 1 < c1)
-                    ptx::tmem_ld_32x32b_x16(t_row + (cc + 1) * 32, va);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    hs[i][8 + q] = zero ? 0u : pack(__uint_as_float(vb[2 * q]), __uint_as_float(vb[2 * q + 1]));
+                for (int q = 0; q < 16; ++q)
+                    hs[i][q] = zero ? 0u : pack(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
             }
         }
         if (release_bar != 0) {
@@ -1517,7 +1515,7 @@ cudaError_t launch_cap(const GemmLaunch &cfg, const GroupArgs *groups, const Wor
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     lc.attrs = attr;
-    lc.numAttrs = CLU ? 2 : 1;
+    lc.numAttrs = (CLU || cfg.pair_launch) ? 2 : 1;
     return cudaLaunchKernelEx(&lc, grouped_gemm_kernel<BN, CAP, DEV, CLU>, prm);
 }
 

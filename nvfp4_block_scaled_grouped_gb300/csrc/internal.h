@@ -192,6 +192,9 @@ struct GemmLaunch {
     bool device_table;      // the group table is `dt` (device memory), not the host array
     int cluster;            // clusters of two CTAs (256 x 256 tiles, whole tiles only; grid = 2 x clusters):
                             // 0 none, 1 CTA pair with cta_group::2 MMAs, 2 multicast cluster
+    bool pair_launch = false;  // cluster == 0: launch the CTAs as clusters of two all the same (placement
+                               // only: the two CTAs of an SM pair take neighbouring tiles, which share
+                               // a B panel; measured 1-2% faster on the ring-bound workloads)
     DeviceTable dt;
 };
 
