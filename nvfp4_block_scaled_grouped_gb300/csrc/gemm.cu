@@ -360,6 +360,9 @@ struct Cursor {
         w += s.kt1 - s.kt0;
     }
 
+    // Whether next() would return another segment.
+    __device__ __forceinline__ bool more() const { return tile < tile_end || w < w_end; }
+
     __device__ __forceinline__ bool next(const GemmParams<CAP, DEV> &p, Segment &s) {
         if (phase == 0) {
             phase = 1;
@@ -1346,10 +1349,9 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
         auto cur = cursor0;
         Segment sg;
         const bool have = cur.next(p, sg);
-        while (have) {
-            Segment nx;
-            if (!cur.next(p, nx))
-                break;
+        // (whether another segment follows is read from the cursor, so the
+        // next segment is not held in registers across this one's epilogue)
+        while (have && cur.more()) {
             const GInfo gi = group_info<BN, CLUSTER>(load_group(p, sg.g));
             // a first piece of a split tile is always a CTA's last segment
             const int kind = sg.kt0 > 0 ? kEpiCont : kEpiWhole;
@@ -1397,7 +1399,7 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                 acc_phase ^= 1u;
             }
             ++it;
-            sg = nx;
+            (void)cur.next(p, sg);
         }
         if (threadIdx.x == 0) {
             s_tail->seg = sg;
