@@ -132,6 +132,37 @@ def test_edge_shapes_full(nv, oracle_mod, monkeypatch, block_n, split):
         assert_parity(c, r, f"edge group {g} {(m, n, k)}")
 
 
+@pytest.mark.parametrize("block_n,split", [(128, False), (256, False), (256, True), (128, True)])
+def test_c_16_byte_aligned_only(nv, oracle_mod, monkeypatch, block_n, split):
+    """C that is 16-byte aligned (what the API requires) but not 32-byte
+    aligned: the epilogue then stores 16-byte pieces instead of 32-byte ones.
+    Results match the oracle on every path that stores fp16 (whole tiles in
+    the main loop and as a CTA's last segment, and the finishing piece of a
+    split tile), and the bytes around each C stay untouched."""
+    from nvfp4_block_scaled_grouped_gb300.device import DeviceProblem, SENTINEL_F16
+    _schedule(monkeypatch, split)
+    sizes = [(200, 320, 512, 1), (64, 256, 768, 1), (300, 512, 256, 1), (129, 96, 7168, 1)]
+    prob = _make(sizes, seed=11)
+    nv.set_tile_n(block_n)
+    dp = DeviceProblem.upload(prob)
+    bufs = []
+    for g, (m, n, _k, _l) in enumerate(sizes):
+        buf = torch.full((m * n + 16,), SENTINEL_F16, dtype=torch.int16, device="cuda")
+        c = buf[8:8 + m * n].view(m, n).view(torch.float16)
+        assert c.data_ptr() % 32 == 16
+        dp.C[g] = c
+        bufs.append(buf)
+    dp.run()
+    torch.cuda.synchronize()
+    assert nv.device_status() == 0
+    ref = _oracle_full(oracle_mod, prob)
+    for g, ((m, n, _k, _l), buf, r) in enumerate(zip(sizes, bufs, ref)):
+        raw = buf.cpu().numpy()
+        assert np.all(raw[:8].view(np.uint16) == SENTINEL_F16), f"group {g}: bytes before C written"
+        assert np.all(raw[8 + m * n:].view(np.uint16) == SENTINEL_F16), f"group {g}: bytes after C written"
+        assert_parity(raw[8:8 + m * n].view(np.float16).reshape(m, n), r, f"16-byte aligned C, group {g}")
+
+
 def test_interior_empty_groups_keep_sentinel(nv, oracle_mod):
     """Empty groups between non-empty ones get no tiles and keep their C; the
     tiles of the neighbours land in the right group."""
