@@ -125,8 +125,10 @@ struct Cfg {
     static constexpr int kMaxLoopChunks = BN / 64;  // column chunks per epilogue warp in the loop
     // barrier area: full / empty / scales-written per stage and the
     // accumulator barriers from 0, scratch from 176, scales-landed per stage
-    // from 384
-    static constexpr int kBarrierBytes = 448;
+    // from 384, the epilogue warps' schedule cursor (64 bytes), two segment
+    // slots (2 x 32) and three flags from 448
+    static constexpr int kBarrierBytes = 640;
+    static constexpr int kEpiCursorOffset = 448;
     static_assert((3 * kStages + 2 * kAccStages) * 8 <= 176 && kStages <= 8, "barrier area");
     // A finishing CTA receives the next piece's partial tile in ring stages,
     // kPartialChunksPerStage 16 KiB chunks (32 columns x 128 rows fp32) per
@@ -1346,22 +1348,37 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
         int acc = 0, it = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        auto cur = cursor0;
-        Segment sg;
-        const bool have = cur.next(p, sg);
-        // (whether another segment follows is read from the cursor, so the
-        // next segment is not held in registers across this one's epilogue)
-        while (have && cur.more()) {
+        // The eight warps' schedule cursor is one copy in shared memory,
+        // advanced by thread 0 (segments in two slots by parity, each with
+        // whether another segment follows it), so that no epilogue register
+        // holds it across the accumulator drain.
+        static_assert(sizeof(Cursor<BN, CAP, DEV, CLUSTER>) <= 64 && 2 * sizeof(Segment) <= 64, "cursor area");
+        auto *ecur = reinterpret_cast<Cursor<BN, CAP, DEV, CLUSTER> *>(bar_area + C::kEpiCursorOffset);
+        Segment *eseg = reinterpret_cast<Segment *>(bar_area + C::kEpiCursorOffset + 64);
+        volatile int *emore = reinterpret_cast<volatile int *>(bar_area + C::kEpiCursorOffset + 128);
+        if (threadIdx.x == 0) {
+            *ecur = cursor0;
+            emore[2] = ecur->next(p, eseg[0]) ? 1 : 0;
+            emore[0] = ecur->more() ? 1 : 0;
+        }
+        ptx::named_barrier(4, 256);
+        const bool have = emore[2] != 0;
+        while (have && emore[it & 1]) {
+            const Segment sg = eseg[it & 1];
             const GInfo gi = group_info<BN, CLUSTER>(load_group(p, sg.g));
             // a first piece of a split tile is always a CTA's last segment
             const int kind = sg.kt0 > 0 ? kEpiCont : kEpiWhole;
-            // One thread waits for the accumulator; the eight warps leave or
-            // stay together (the TMEM loads are warp-collective).
-            if (threadIdx.x == 0)
+            // One thread takes the next segment and waits for the
+            // accumulator; the eight warps leave or stay together (the TMEM
+            // loads are warp-collective).
+            if (threadIdx.x == 0) {
+                (void)ecur->next(p, eseg[(it + 1) & 1]);
+                emore[(it + 1) & 1] = ecur->more() ? 1 : 0;
                 s_epi_ok[it & 1] = wait_bounded(accf_bar(acc), acc_phase, abort_flag, p.timeout_ns, p.ws.status,
                                                 kStatusEpilogueTimeout, peer_abort, remote_accf)
                                        ? 1
                                        : 0;
+            }
             ptx::named_barrier(4, 256);
             if (!s_epi_ok[it & 1]) {
                 ok = false;
@@ -1399,10 +1416,9 @@ __global__ void __launch_bounds__(448, 1) grouped_gemm_kernel(const __grid_const
                 acc_phase ^= 1u;
             }
             ++it;
-            (void)cur.next(p, sg);
         }
         if (threadIdx.x == 0) {
-            s_tail->seg = sg;
+            s_tail->seg = eseg[it & 1];
             s_tail->valid = (have && ok) ? 1 : 0;
             s_tail->acc = acc;
             s_tail->acc_phase = (int32_t)acc_phase;
