@@ -28,7 +28,9 @@
 // cover the padded rows (a multiple of 128) and the padded scale blocks (a
 // multiple of 4), whose scale bytes are written as zero. Warps walk the units
 // grid-stride, two units per step so that two loads of each lane are in
-// flight. The kernel streams its input once (bound by HBM bandwidth for large
+// flight. The quotients are formed two at a time with the packed fp32
+// instructions (mul / fma .f32x2, each lane the IEEE operation of its scalar
+// form). The kernel streams its input once (bound by HBM bandwidth for large
 // inputs).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -111,6 +113,22 @@ __device__ __forceinline__ float div_corrected(float x, float d, float r) {
     return fmaf(fmaf(-q0, d, x), r, q0);
 }
 
+// The same step for two dividends x0, x1 over one divisor d (nd = -d), with
+// the packed fp32 instructions: q0 = x * r, e = q0 * (-d) + x, q = e * r + q0,
+// each rounded to nearest even per lane as the scalar mul / fma are.
+__device__ __forceinline__ void div_corrected2(float x0, float x1, float nd, float r, float &q0, float &q1) {
+    asm("{\n\t.reg .b64 xx, rr, dd, q, e;\n\t"
+        "mov.b64 xx, {%2, %3};\n\t"
+        "mov.b64 rr, {%4, %4};\n\t"
+        "mov.b64 dd, {%5, %5};\n\t"
+        "mul.rn.f32x2 q, xx, rr;\n\t"
+        "fma.rn.f32x2 e, q, dd, xx;\n\t"
+        "fma.rn.f32x2 q, e, rr, q;\n\t"
+        "mov.b64 {%0, %1}, q;\n\t}"
+        : "=f"(q0), "=f"(q1)
+        : "f"(x0), "f"(x1), "f"(r), "f"(nd));
+}
+
 // Hardware reciprocal estimate (PTX rcp.approx, about 1 ulp); d here is an
 // e4m3 value in [2^-9, 448], a normal fp32 number.
 __device__ __forceinline__ float rcp_estimate(float d) {
@@ -122,7 +140,7 @@ __device__ __forceinline__ float rcp_estimate(float d) {
 // Quantise one 16-element block: its e4m3 scale code, and its 16 e2m1 codes
 // packed into 8 bytes (element j in bits 4j..4j+3).
 //
-// amax / 6 and the quotients x / dec come from div_corrected: exact on every
+// amax / 6 and the quotients x / dec come from div_corrected(2): exact on every
 // quotient that is representable -- in particular on every e4m3 rounding
 // midpoint amax / 6 and every e2m1 rounding boundary x / dec = t -- so those
 // ties are decided by round-to-nearest-even as for the exact quotient; every
@@ -143,10 +161,11 @@ __device__ __forceinline__ uint32_t quantize16(const float (&f)[16], uint2 &pack
         for (int h = 0; h < 2; ++h) {
             float q[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float x = f[8 * h + j];
+            for (int j = 0; j < 8; j += 2) {
+                div_corrected2(f[8 * h + j], f[8 * h + j + 1], -dec, r, q[j], q[j + 1]);
                 // (the correction turns x = -0 into +0; the quotient has x's sign)
-                q[j] = copysignf(div_corrected(x, dec, r), x);
+                q[j] = copysignf(q[j], f[8 * h + j]);
+                q[j + 1] = copysignf(q[j + 1], f[8 * h + j + 1]);
             }
             w[h] = cvt_e2m1x8(q);
         }
