@@ -81,6 +81,7 @@ CASES = [  # (seed, groups, max_m, max_n, max_k, max_l)
     (2, 8, 140, 384, 2048, 2),
     (3, 40, 96, 256, 512, 2),
     (4, 100, 40, 128, 256, 1),
+    (5, 512, 24, 64, 128, 1),   # the largest call: NVFP4_MAX_GROUPS groups
 ]
 
 
