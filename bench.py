@@ -100,24 +100,32 @@ def kernel_code_digest(path) -> str:
     return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
 
 
-def stored_traffic(workload, tile_n):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the kernel code as it is now (else None)."""
-    summ = ROOT / "profiles" / f"gemm_kernel_{workload}.txt"
+def profile_traffic(summary, source, expect=None):
+    """DRAM bytes per launch from a committed ncu summary under profiles/, if it
+    was taken on the kernel source as it is now and with the settings in
+    `expect` (else None)."""
+    summ = ROOT / "profiles" / summary
     if not summ.exists():
         return None
-    digest = kernel_code_digest(ROOT / "nvfp4_block_scaled_grouped_gb300" / "csrc" / "gemm.cu")
+    digest = kernel_code_digest(ROOT / "nvfp4_block_scaled_grouped_gb300" / "csrc" / source)
     kv = {}
     for line in summ.read_text().splitlines():
         if ": " in line:
             k, v = line.split(": ", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("gemm.cu code sha256[:16]", "").split(" ")[0] != digest or kv.get("tile_n") != str(tile_n):
+    if kv.get(f"{source} code sha256[:16]", "").split(" ")[0] != digest:
+        return None
+    if any(kv.get(k) != v for k, v in (expect or {}).items()):
         return None
     try:
         return float(kv["dram bytes per launch"])
     except (KeyError, ValueError):
         return None
+
+
+def stored_traffic(workload, tile_n):
+    """The grouped GEMM kernel's DRAM bytes per launch for a workload."""
+    return profile_traffic(f"gemm_kernel_{workload}.txt", "gemm.cu", {"tile_n": str(tile_n)})
 
 
 class ClockSampler:
@@ -612,7 +620,8 @@ def quantize_arm(args, rank, world, local_rank):
     t_s = t_ms * 1e-3
     roof = {"bound": "hbm", "achieved": nbytes / t_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = profile_traffic(f"quantize_pack_kernel_{args.workload}.txt", "quantize.cu",
+                                      {"rows": str(rows), "k": str(k)})
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
     roof["kernel"] = "quantize_pack_kernel (the only kernel of the call)"
     cpu = None

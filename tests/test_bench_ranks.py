@@ -101,3 +101,25 @@ def test_profile_summary_lookup(tmp_path, monkeypatch):
     assert bench.stored_traffic("decode", 128) is None
     summ.write_text("gemm.cu code sha256[:16]: 0000000000000000\ntile_n: 256\ndram bytes per launch: 1\n")
     assert bench.stored_traffic("decode", 256) is None
+
+
+def test_quantize_traffic_names_its_own_source(tmp_path, monkeypatch):
+    """The quantise line's `traffic` checks quantize.cu's digest and the
+    profiled shape, not the GEMM kernel's."""
+    sys.path.insert(0, str(ROOT))
+    import bench
+    csrc = tmp_path / "nvfp4_block_scaled_grouped_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "quantize.cu").write_text("__global__ void q() {}\n")
+    (csrc / "gemm.cu").write_text("__global__ void g() {}\n")
+    dq = bench.kernel_code_digest(csrc / "quantize.cu")
+    dg = bench.kernel_code_digest(csrc / "gemm.cu")
+    summ = tmp_path / "profiles" / "quantize_pack_kernel_prefill.txt"
+    monkeypatch.setattr(bench, "ROOT", tmp_path)
+    shape = {"rows": "8192", "k": "7168"}
+    summ.write_text(f"quantize.cu code sha256[:16]: {dq}\nrows: 8192\nk: 7168\ndram bytes per launch: 777\n")
+    assert bench.profile_traffic("quantize_pack_kernel_prefill.txt", "quantize.cu", shape) == 777.0
+    assert bench.profile_traffic("quantize_pack_kernel_prefill.txt", "quantize.cu", {"rows": "732", "k": "7168"}) is None
+    summ.write_text(f"gemm.cu code sha256[:16]: {dg}\nrows: 8192\nk: 7168\ndram bytes per launch: 777\n")
+    assert bench.profile_traffic("quantize_pack_kernel_prefill.txt", "quantize.cu", shape) is None
