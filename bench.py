@@ -62,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--flush-mb", type=int, default=512, help="L2 flush buffer read between timed calls")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-streams", type=int, default=1,
+                    help="streams each e2e host<->device copy is split over (copy engines in parallel)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target wall time of the oracle sample")
     return ap.parse_args(argv)
 
@@ -482,25 +484,50 @@ def gpu_arm(args, rank, world, local_rank):
         call_e2e = make_call(q)
         h2d, d2h = in_bytes, out_bytes
         e2e_steps = max(3, min(args.steps, 10))
+        side = [torch.cuda.Stream(dev) for _ in range(max(1, args.e2e_streams) - 1)]
+
+        def copy(dst, src):
+            # dst.copy_(src) in 256-byte-aligned contiguous pieces, one per
+            # stream (the launching stream's own included), joined back on it
+            n = len(side) + 1
+            per = -(-dst.numel() // n)
+            piece = -(-per // 256) * 256
+            start = torch.cuda.Event()
+            start.record(stream)
+            joins = []
+            for i, st in enumerate(side, 1):
+                lo, hi = i * piece, min((i + 1) * piece, dst.numel())
+                if lo >= hi:
+                    break
+                st.wait_event(start)
+                with torch.cuda.stream(st):
+                    dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(st)
+                joins.append(e)
+            dst[:piece].copy_(src[:piece], non_blocking=True)
+            for e in joins:
+                stream.wait_event(e)
+
         for _ in range(2):
-            d_in.copy_(h_in, non_blocking=True)
+            copy(d_in, h_in)
             call_e2e()
-            h_out.copy_(d_out, non_blocking=True)
+            copy(h_out, d_out)
         torch.cuda.synchronize()
         e_ms = []
         for _ in range(e2e_steps):
             flush.sum()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            d_in.copy_(h_in, non_blocking=True)
+            copy(d_in, h_in)
             call_e2e()
-            h_out.copy_(d_out, non_blocking=True)
+            copy(h_out, d_out)
             b.record(stream)
             b.synchronize()
             e_ms.append(a.elapsed_time(b))
         em = max_over_ranks(statistics.fmean(e_ms), world, dev)
         e2e = {"value": replica_throughput(flops, world, em * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": em, "steps": e2e_steps}
+               "d2h_bytes_per_step": d2h, "ms_per_step": em, "steps": e2e_steps, "copy_streams": len(side) + 1}
 
     if rank != 0:
         return 0
