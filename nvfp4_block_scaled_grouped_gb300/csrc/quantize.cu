@@ -177,7 +177,8 @@ __device__ __forceinline__ uint32_t quantize16(const float (&f)[16], uint2 &pack
 template <bool BF16>
 __global__ void __launch_bounds__(kQuantThreads) quantize_pack_kernel(const uint16_t *__restrict__ x, int rows, int k,
                                                                       uint8_t *__restrict__ codes,
-                                                                      uint8_t *__restrict__ sf_atoms) {
+                                                                      uint8_t *__restrict__ sf_atoms,
+                                                                      uint32_t chunks_m, int chunks_s) {
     const int lane = threadIdx.x & 31;
     const int k_blocks = k / 16;
     const int k_atoms = (k + 63) / 64;
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_pack_kernel(const uint
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int u = u0 + i * stride;
-            r[i] = u / chunks;
+            r[i] = (int)(((uint64_t)(uint32_t)u * chunks_m) >> chunks_s);  // u / chunks
             kb[i] = (u - r[i] * chunks) * kUnitBlocks + lane;
             real[i] = u < units && r[i] < rows && kb[i] < k_blocks;
             const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)r[i] * (size_t)k + (size_t)kb[i] * 16);
@@ -218,9 +219,9 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_pack_kernel(const uint
             word |= __shfl_down_sync(full, sc, 2) << 16;
             word |= __shfl_down_sync(full, sc, 3) << 24;
             if ((lane & 3) == 0 && kb[i] < blocks_pad) {
-                const int rr = r[i];
-                uint8_t *atom = sf_atoms + ((size_t)(rr / 128) * (size_t)k_atoms + (size_t)(kb[i] / 4)) * kSfAtomBytes;
-                *reinterpret_cast<uint32_t *>(atom + 16 * (rr % 32) + 4 * ((rr / 32) % 4)) = word;
+                const uint32_t rr = (uint32_t)r[i];
+                uint8_t *atom = sf_atoms + ((size_t)(rr >> 7) * (size_t)k_atoms + (size_t)((uint32_t)kb[i] >> 2)) * kSfAtomBytes;
+                *reinterpret_cast<uint32_t *>(atom + 16 * (rr & 31u) + 4 * ((rr >> 5) & 3u)) = word;
             }
         }
     }
@@ -243,13 +244,21 @@ cudaError_t launch_quantize_pack(const void *x, bool bf16, int rows, int k, void
     // enough resident warps to keep two 512-byte loads each in flight
     const long long want = (units + kQuantThreads / 32 - 1) / (kQuantThreads / 32);
     const int grid = (int)(want < 8LL * sms ? want : 8LL * sms);
+    // unit u's row u / chunks by multiplication: with l = ceil(log2 chunks)
+    // and m = ceil(2^(31+l) / chunks), floor(u / chunks) = (u * m) >> (31 + l)
+    // for every u < 2^31 (Granlund and Montgomery, "Division by Invariant
+    // Integers using Multiplication", Theorem 4.2); m < 2^32
+    int l = 0;
+    while ((1LL << l) < chunks)
+        ++l;
+    const uint32_t chunks_m = (uint32_t)((((uint64_t)1 << (31 + l)) + (uint64_t)chunks - 1) / (uint64_t)chunks);
     const uint16_t *xs = static_cast<const uint16_t *>(x);
     uint8_t *c = static_cast<uint8_t *>(codes);
     uint8_t *s = static_cast<uint8_t *>(sf_atoms);
     if (bf16)
-        quantize_pack_kernel<true><<<grid, kQuantThreads, 0, stream>>>(xs, rows, k, c, s);
+        quantize_pack_kernel<true><<<grid, kQuantThreads, 0, stream>>>(xs, rows, k, c, s, chunks_m, 31 + l);
     else
-        quantize_pack_kernel<false><<<grid, kQuantThreads, 0, stream>>>(xs, rows, k, c, s);
+        quantize_pack_kernel<false><<<grid, kQuantThreads, 0, stream>>>(xs, rows, k, c, s, chunks_m, 31 + l);
     return cudaGetLastError();
 }
 
