@@ -174,6 +174,8 @@ __device__ __forceinline__ uint32_t quantize16(const float (&f)[16], uint2 &pack
     return sc;
 }
 
+// chunks_m, chunks_s: the host's multiplier and shift that divide a unit
+// index by the units per row (see launch_quantize_pack).
 template <bool BF16>
 __global__ void __launch_bounds__(kQuantThreads) quantize_pack_kernel(const uint16_t *__restrict__ x, int rows, int k,
                                                                       uint8_t *__restrict__ codes,
